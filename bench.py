@@ -1,0 +1,523 @@
+"""Benchmark of the hybrid tree attention hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch: the tree mask build
+(hta_build_mask) and the fused verification attention (hta_verify: split-KV
+pass over the cache, masked pass over the tree, log-sum-exp merge). The
+workload is the LLaMA-3.1-8B layer shape at a 32K context (B=1, Hq=32, Hkv=8,
+d=128, L=32768, T=64, depth <= 8 tree) with seeded N(0,1) bf16 values.
+
+Inputs are resident in HBM before the timed region. The step cycles over
+several independently drawn K/V caches whose total size exceeds the 129 MB
+L2, so each step reads its cache from HBM. Steps are replayed from a CUDA
+graph (one graph holds one step per cache), so host launch cost stays out of
+the device-timed loop.
+
+Output: one JSON line (rank 0). `value` is KV-cache GB/s over the whole job
+(all ranks); `us_per_layer_call` the mean hta_verify duration from CUDA events
+on the launching stream; `roofline` compares that kernel with the measured HBM
+copy bandwidth; `e2e` repeats the measurement through the public API with the
+inputs in pinned host memory (copies inside the timed region); `cpu_baseline`
+times the fp64 CPU oracle on a bounded sample.
+
+--impl reference times the CPU oracle alone on the host cores (the reference
+arm: there is no runnable reference implementation of this method).
+With torchrun (WORLD_SIZE > 1) every rank runs an independent replica on its
+own GPU: the path shards by sequence and KV head with no exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from speculative_decoding_tree_hybrid_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "tree-verify attn µs/layer-call and HBM GB/s (% of roofline) at L=32K"
+FALLBACK_HBM_GBS = 6800.0
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# --------------------------------------------------------------------------- helpers
+
+def kv_bytes(inp) -> int:
+    """Algorithmic KV-cache bytes of one layer-call: every cached K and V row once."""
+    cfg = inp.cfg
+    return int(np.sum(inp.cache_lens.astype(np.int64))) * cfg.Hkv * cfg.d * 2 * 2
+
+
+def all_bytes(inp) -> int:
+    """KV bytes plus the tree K/V, q, o (bf16), lse (fp32) and the mask."""
+    cfg = inp.cfg
+    W = (cfg.T + 31) // 32
+    return (kv_bytes(inp) + 2 * cfg.B * cfg.Hkv * cfg.T * cfg.d * 2 + 2 * cfg.B * cfg.T * cfg.Hq * cfg.d * 2
+            + cfg.B * cfg.T * cfg.Hq * 4 + cfg.B * cfg.T * W * 4)
+
+
+def workload_desc(cfg) -> str:
+    L = f"L={cfg.L}" if cfg.L is not None else f"L~U{list(cfg.L_range)}"
+    return (f"{cfg.name}: B={cfg.B} Hq={cfg.Hq} Hkv={cfg.Hkv} d={cfg.d} {L} T={cfg.T} "
+            f"tree={cfg.tree} bf16 N(0,1) post-RoPE, scale 1/sqrt(d)")
+
+
+def measured_peak():
+    try:
+        with open(PEAKS_FILE) as fh:
+            peaks = json.load(fh)
+        return float(peaks["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_hybrid_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """Per-launch DRAM bytes from a committed ncu summary, only if it was taken
+    on the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            rec = json.load(fh)
+        e = rec[workload]
+        if e.get("kernel") == kernel and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def reduce_max(pg, value: float, device=None) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg, device=None):
+    if pg is None:
+        return
+    if device is not None and device.type == "cuda":
+        pg.barrier(device_ids=[device.index])
+    else:
+        pg.barrier()
+
+
+def aggregate(units_per_rank: float, elapsed_s: float, pg, device=None):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    world = 1 if pg is None else pg.get_world_size()
+    t = reduce_max(pg, elapsed_s, device)
+    return units_per_rank * world / t, t
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(inp, rows_target: int, seconds: float):
+    """Times the fp64 oracle on whole layer-calls' worth of rows.
+
+    Returns (seconds per full layer-call (extrapolated), threads, description).
+    """
+    import oracle
+    cfg = inp.cfg
+    total_rows = cfg.B * cfg.T * cfg.Hq
+    mask, _ = oracle.build_mask(inp.parents)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(total_rows, size=min(rows_target, total_rows), replace=False))
+    done_rows, t_used, calls = 0, 0.0, 0
+    while t_used < seconds or calls == 0:
+        t0 = time.perf_counter()
+        oracle.attention(inp.q, inp.k_cache, inp.v_cache, inp.cache_lens, inp.k_spec, inp.v_spec,
+                         mask, rows=rows)
+        t_used += time.perf_counter() - t0
+        done_rows += rows.size
+        calls += 1
+    per_call = t_used / done_rows * total_rows
+    desc = (f"{calls} x {rows.size} of {total_rows} query rows (fp64 oracle, OpenMP over rows), "
+            f"{t_used:.1f} s total, extrapolated to one full layer-call")
+    return per_call, oracle.num_threads(), desc, t_used, done_rows
+
+
+def run_reference(args, world, rank, pg):
+    if rank != 0:
+        return
+    cfg = wl.CONFIGS[args.config]
+    inp = wl.make_inputs(cfg, threads=os.cpu_count() or 8)
+    total_rows = cfg.B * cfg.T * cfg.Hq
+    rows_per_step = max(1, min(total_rows, args.ref_rows))
+    import oracle
+    mask, _ = oracle.build_mask(inp.parents)
+    rows = np.sort(np.random.default_rng(0).choice(total_rows, size=rows_per_step, replace=False))
+    for _ in range(args.warmup):
+        oracle.attention(inp.q, inp.k_cache, inp.v_cache, inp.cache_lens, inp.k_spec, inp.v_spec,
+                         mask, rows=rows[: max(1, rows_per_step // 8)])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(inp.q, inp.k_cache, inp.v_cache, inp.cache_lens, inp.k_spec, inp.v_spec,
+                         mask, rows=rows)
+    el = time.perf_counter() - t0
+    per_call = el / (args.steps * rows_per_step) * total_rows
+    value = kv_bytes(inp) / per_call / 1e9
+    sample = (f"each step: {rows_per_step} of {total_rows} query rows of one layer-call; "
+              f"value extrapolates to the full layer-call")
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3),
+        "us_per_layer_call": round(per_call * 1e6, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(cfg)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, world, rank, local, pg):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_tree_hybrid_gb300 import hta
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CONFIGS[args.config]
+    n_sets = args.kv_sets
+    sets = [wl.make_inputs(cfg, kv_set=k, threads=os.cpu_count() or 8) for k in range(n_sets)]
+    base = sets[0]
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q = bf16(base.q)
+    ks, vs = bf16(base.k_spec), bf16(base.v_spec)
+    lens = torch.from_numpy(base.cache_lens).to(dev)
+    parents = torch.from_numpy(base.parents).to(dev)
+    kcs = [bf16(s.k_cache) for s in sets]
+    vcs = [bf16(s.v_cache) for s in sets]
+    dims = hta.dims_of(q, kcs[0])
+    ws = hta.workspace(dims, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    mask = torch.empty((cfg.B, cfg.T, (cfg.T + 31) // 32), dtype=torch.int32, device=dev)
+
+    stream = torch.cuda.Stream(dev)
+
+    def one_step(k):
+        hta.build_mask(parents, dev_err=err, out=mask)
+        hta.verify(q, kcs[k], vcs[k], lens, ks, vs, mask, ws=ws, dev_err=err, out=(o, lse))
+
+    # one graph replays one step per K/V set
+    graph = None
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for k in range(n_sets):
+                one_step(k)
+        torch.cuda.synchronize(dev)
+        path = hta.last_path()
+        if not args.no_graph:
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    for k in range(n_sets):
+                        one_step(k)
+                graph = g
+            except Exception as e:  # capture unsupported: time eager launches instead
+                print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
+                graph = None
+                torch.cuda.synchronize(dev)
+
+    def run_steps(n):
+        with torch.cuda.stream(stream):
+            for _ in range(n // n_sets):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    for k in range(n_sets):
+                        one_step(k)
+
+    # warm-up
+    run_steps(max(args.warmup, 3) * n_sets)
+    torch.cuda.synchronize(dev)
+    steps = (args.steps + n_sets - 1) // n_sets * n_sets
+
+    # per-launch hta_verify duration (CUDA events on the launching stream).
+    # A 512 MB memset ahead of each launch flushes L2 and keeps the stream
+    # busy while the events and the kernel are enqueued.
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    n_meas = max(4, min(args.launch_samples, steps))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_meas)]
+    with torch.cuda.stream(stream):
+        for i in range(n_meas):
+            k = i % n_sets
+            flush.fill_(i & 0xFF)
+            hta.build_mask(parents, dev_err=err, out=mask)
+            ev[i][0].record(stream)
+            hta.verify(q, kcs[k], vcs[k], lens, ks, vs, mask, ws=ws, dev_err=err, out=(o, lse))
+            ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    us_call = statistics.median(per_launch_ms) * 1e3
+    del flush
+
+    # timed region
+    err.zero_()
+    barrier(pg, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        run_steps(steps)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(pg, dev)
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    dev_err = int(err.item())
+    if dev_err:
+        raise SystemExit(f"device error flags {dev_err}")
+
+    bytes_step = kv_bytes(base)
+    gbs, t_max = aggregate(bytes_step * steps / 1e9, elapsed, pg, dev)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, hta, sets, dev, pg)
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    achieved = bytes_step / (us_call * 1e-6) / 1e9
+    kernel = "k_tc_verify" if path == hta.PATH_TC else "k_cc_attn"
+    traffic = recorded_traffic(cfg.name, kernel)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        per_call, cores, desc, _, _ = oracle_sample(base, args.cpu_rows, args.cpu_seconds)
+        cpu = {"value": round(bytes_step / per_call / 1e9, 4), "unit": "GB/s", "cores": cores,
+               "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": max(args.warmup, 3) * n_sets,
+        "ms_per_step": round(t_max / steps * 1e3, 5),
+        "us_per_layer_call": round(us_call, 3),
+        "us_per_layer_call_p10_p90": [round(float(np.percentile(per_launch_ms, 10)) * 1e3, 3),
+                                      round(float(np.percentile(per_launch_ms, 90)) * 1e3, 3)],
+        "pct_hbm_roofline": round(100.0 * achieved / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "kv_sets": n_sets,
+                   "l2": f"{n_sets} K/V caches of {bytes_step / 1e6:.1f} MB rotated (> 129 MB L2)",
+                   "graph": graph is not None, "path": "tcgen05" if path == hta.PATH_TC else "cuda-core",
+                   "all_bytes_per_call": all_bytes(base)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": kernel, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": bytes_step},
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "gpu_launches": 2 * steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, hta, sets, dev, pg):
+    """Same metric through the public API, inputs in pinned host memory: every
+    step copies its inputs host->device, runs mask + verify, and reads o and
+    lse back."""
+    import torch
+    base = sets[0]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    h_q, h_ks, h_vs = pin(base.q), pin(base.k_spec), pin(base.v_spec)
+    h_lens = torch.from_numpy(base.cache_lens).pin_memory()
+    h_par = torch.from_numpy(base.parents).pin_memory()
+    h_kc = [pin(s.k_cache) for s in sets[:2]]
+    h_vc = [pin(s.v_cache) for s in sets[:2]]
+    d = lambda h: torch.empty(h.shape, dtype=h.dtype, device=dev)
+    d_q, d_ks, d_vs, d_lens, d_par = d(h_q), d(h_ks), d(h_vs), d(h_lens), d(h_par)
+    d_kc, d_vc = d(h_kc[0]), d(h_vc[0])
+    h_o = torch.empty(base.q.shape, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(base.q.shape[:3], dtype=torch.float32).pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    bf = lambda t: t.view(torch.bfloat16)
+    dims = hta.dims_of(bf(d_q), bf(d_kc))
+    ws = hta.workspace(dims, dev)
+    o = torch.empty(base.q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(base.q.shape[:3], dtype=torch.float32, device=dev)
+    mask = torch.empty((base.cfg.B, base.cfg.T, (base.cfg.T + 31) // 32), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_ks, h_vs, h_lens, h_par, h_kc[0], h_vc[0]))
+    d2h = h_o.numel() * 2 + h_lse.numel() * 4
+
+    def one(k):
+        for dst, src in ((d_q, h_q), (d_ks, h_ks), (d_vs, h_vs), (d_lens, h_lens), (d_par, h_par),
+                         (d_kc, h_kc[k % 2]), (d_vc, h_vc[k % 2])):
+            dst.copy_(src, non_blocking=True)
+        hta.build_mask(d_par, dev_err=err, out=mask)
+        hta.verify(bf(d_q), bf(d_kc), bf(d_vc), d_lens, bf(d_ks), bf(d_vs), mask, ws=ws, dev_err=err,
+                   out=(o, lse))
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    steps = max(4, min(args.e2e_steps, args.steps))
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            one(k)
+        torch.cuda.synchronize(dev)
+        barrier(pg, dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(steps):
+            one(k)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(pg, dev)
+    el = t0.elapsed_time(t1) / 1e3
+    gbs, t_max = aggregate(kv_bytes(base) * steps / 1e9, el, pg, dev)
+    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": round(t_max / steps * 1e3, 4)}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["hta", "reference"], default="hta")
+    ap.add_argument("--config", default="llama8b", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--kv-sets", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--launch-samples", type=int, default=200)
+    ap.add_argument("--cpu-rows", type=int, default=2048)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local, pg = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, pg)
+        else:
+            run_gpu(args, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,291 @@
+// C-ABI entry points of libhta: argument checks, workspace layout, kernel-path
+// choice and launches. Every step of the computation runs in the kernels of
+// k_mask.cu, k_cc.cu, k_tc.cu and k_merge.cu; this file only validates and
+// dispatches.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "hta_launch.h"
+
+using hta::AttnParams;
+
+namespace {
+
+thread_local int32_t g_last_path = 0;
+
+constexpr size_t kWsAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int num_sms_current() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+bool tc_device_ok() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    return major == 10 && minor == 3;
+}
+
+hta_status check_dims(const hta_dims *d) {
+    if (!d) return HTA_ERR_INVALID_ARG;
+    if (d->B <= 0 || d->T <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->d <= 0 || d->Lmax < 0)
+        return HTA_ERR_INVALID_ARG;
+    if (!(d->scale >= 0.f) || isinf(d->scale)) return HTA_ERR_INVALID_ARG;
+    if (d->Hq % d->Hkv != 0) return HTA_ERR_UNSUPPORTED;
+    if (d->d != 64 && d->d != 128) return HTA_ERR_UNSUPPORTED;
+    if (d->T > HTA_TMAX || d->B > HTA_BMAX) return HTA_ERR_UNSUPPORTED;
+    if (d->Lmax > (int64_t)0x7fffffff) return HTA_ERR_UNSUPPORTED;
+    return HTA_OK;
+}
+
+enum Path { kPathNone = 0, kPathCC = 1, kPathTC = 2 };
+
+// Environment override HTA_FORCE_PATH=cc|tc, read on every call.
+int forced_path() {
+    const char *s = getenv("HTA_FORCE_PATH");
+    if (!s) return kPathNone;
+    if (!strcmp(s, "cc")) return kPathCC;
+    if (!strcmp(s, "tc")) return kPathTC;
+    return kPathNone;
+}
+
+// Tensor cores when the head dimension is 128 and the packed query rows of
+// a KV head (T*G) are enough for a dense 128-row MMA tile to be worth it.
+int choose_path(const hta_dims *d) {
+    const int forced = forced_path();
+    const bool tc_ok = d->d == 128 && tc_device_ok() && hta::tc_rows_per_group() > 0;
+    if (forced == kPathCC) return kPathCC;
+    if (forced == kPathTC) return tc_ok ? kPathTC : kPathNone;
+    const int R = d->T * (d->Hq / d->Hkv);
+    return (tc_ok && R >= 16) ? kPathTC : kPathCC;
+}
+
+struct Layout {
+    int n_rg, rows_pg, tile, n_tree_tiles;
+    int64_t n_seg, slots;
+    size_t off_m, off_l, off_o, total;
+};
+
+Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
+    Layout L = {};
+    const int R = d->T * (d->Hq / d->Hkv);
+    const int rpg_max = path == kPathTC ? hta::tc_rows_per_group() : hta::cc_rows_per_group();
+    L.tile = path == kPathTC ? hta::tc_tile() : hta::cc_tile();
+    L.n_rg = (R + rpg_max - 1) / rpg_max;
+    L.rows_pg = (R + L.n_rg - 1) / L.n_rg;
+    L.n_tree_tiles = tree ? (d->T + L.tile - 1) / L.tile : 0;
+    L.n_seg = (int64_t)d->B * d->Hkv * L.n_rg;
+    L.slots = L.n_seg + grid;
+    size_t off = kWsAlign;  // barrier counters
+    L.off_m = off;
+    off = align_up(off + (size_t)L.slots * L.rows_pg * sizeof(float), kWsAlign);
+    L.off_l = off;
+    off = align_up(off + (size_t)L.slots * L.rows_pg * sizeof(float), kWsAlign);
+    L.off_o = off;
+    off = align_up(off + (size_t)L.slots * L.rows_pg * d->d * sizeof(float), kWsAlign);
+    L.total = off;
+    return L;
+}
+
+int max_grid(int path, const hta_dims *d) {
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    return path == kPathTC ? hta::tc_max_grid(d->B, sms) : hta::cc_max_grid(d->d, d->B, sms);
+}
+
+AttnParams base_params(const hta_dims *d, const Layout &L) {
+    AttnParams p;
+    memset(&p, 0, sizeof p);
+    p.B = d->B;
+    p.T = d->T;
+    p.Hq = d->Hq;
+    p.Hkv = d->Hkv;
+    p.G = d->Hq / d->Hkv;
+    p.d = d->d;
+    p.W = (d->T + 31) / 32;
+    p.Lmax = d->Lmax;
+    const double scale = d->scale > 0.f ? (double)d->scale : 1.0 / sqrt((double)d->d);
+    p.scale_log2 = (float)(scale * 1.4426950408889634);
+    p.R = d->T * p.G;
+    p.n_rg = L.n_rg;
+    p.rows_pg = L.rows_pg;
+    p.tile = L.tile;
+    p.n_tree_tiles = L.n_tree_tiles;
+    return p;
+}
+
+// Runs one attention launch over the cache and/or the tree.
+hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const void *vc,
+                         const int32_t *lens, const void *ks, const void *vs, const uint32_t *mask,
+                         void *out_o, float *out_lse, bool out_fp32, bool use_cache, bool use_tree,
+                         void *ws, size_t ws_bytes, int32_t *dev_err, cudaStream_t stream) {
+    const int path = choose_path(d);
+    if (path == kPathNone) return HTA_ERR_UNSUPPORTED;
+    const int gmax = max_grid(path, d);
+    if (gmax <= 0) return HTA_ERR_CUDA;
+    const bool direct = !use_cache;  // tree-only: one CTA finishes each segment, no workspace
+    Layout L0 = make_layout(d, path, 0, use_tree);
+    const int64_t max_units =
+        L0.n_seg * (int64_t)(L0.n_tree_tiles + (use_cache ? (d->Lmax + L0.tile - 1) / L0.tile : 0));
+    int grid;
+    if (direct)
+        grid = (int)(L0.n_seg < (int64_t)gmax ? L0.n_seg : gmax);
+    else
+        grid = (int)(max_units < (int64_t)gmax ? (max_units > 0 ? max_units : 1) : gmax);
+    Layout L = make_layout(d, path, grid, use_tree);
+    AttnParams p = base_params(d, L);
+    p.q = (const __nv_bfloat16 *)q;
+    p.k_cache = (const __nv_bfloat16 *)kc;
+    p.v_cache = (const __nv_bfloat16 *)vc;
+    p.cache_lens = lens;
+    p.k_spec = (const __nv_bfloat16 *)ks;
+    p.v_spec = (const __nv_bfloat16 *)vs;
+    p.mask = mask;
+    p.out_o = out_o;
+    p.out_lse = out_lse;
+    p.out_fp32 = out_fp32 ? 1 : 0;
+    p.include_cache = use_cache ? 1 : 0;
+    p.include_tree = use_tree ? 1 : 0;
+    p.dev_err = dev_err;
+    if (!direct) {
+        if (!ws || ((uintptr_t)ws % kWsAlign) != 0 || ws_bytes < L.total) return HTA_ERR_WORKSPACE;
+        char *base = (char *)ws;
+        p.bar = (unsigned int *)base;
+        p.ws_m = (float *)(base + L.off_m);
+        p.ws_l = (float *)(base + L.off_l);
+        p.ws_o = (float *)(base + L.off_o);
+        p.slots = L.slots;
+    }
+    cudaError_t e;
+    if (path == kPathTC) {
+        if (direct) return HTA_ERR_UNSUPPORTED;  // tree-only calls take the CUDA-core path
+        e = hta::tc_launch(p, grid, stream);
+    } else {
+        e = hta::cc_launch(p, direct, grid, stream);
+    }
+    if (e != cudaSuccess) return HTA_ERR_CUDA;
+    g_last_path = path;
+    return HTA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hta_status_string(hta_status s) {
+    switch (s) {
+        case HTA_OK: return "ok";
+        case HTA_ERR_INVALID_ARG: return "invalid argument";
+        case HTA_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case HTA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case HTA_ERR_BAD_TREE: return "invalid parent array";
+        case HTA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case HTA_ERR_CUDA: return "CUDA launch failed";
+        case HTA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t hta_last_path(void) { return g_last_path; }
+
+hta_status hta_build_mask(const int32_t *parents, int32_t B, int32_t T, uint32_t *mask,
+                          int32_t *dev_err, cudaStream_t stream) {
+    if (!parents || !mask || B <= 0 || T <= 0) return HTA_ERR_INVALID_ARG;
+    if (T > HTA_TMAX || B > HTA_BMAX) return HTA_ERR_UNSUPPORTED;
+    if (hta::mask_launch(parents, B, T, mask, dev_err, stream) != cudaSuccess) return HTA_ERR_CUDA;
+    return HTA_OK;
+}
+
+size_t hta_workspace_bytes(const hta_dims *d) {
+    if (check_dims(d) != HTA_OK) return 0;
+    size_t best = 0;
+    const int paths[2] = {kPathCC, kPathTC};
+    for (int i = 0; i < 2; ++i) {
+        if (paths[i] == kPathTC && !(d->d == 128 && tc_device_ok() && hta::tc_rows_per_group() > 0)) continue;
+        const int g = max_grid(paths[i], d);
+        if (g <= 0) continue;
+        const Layout L = make_layout(d, paths[i], g, true);
+        if (L.total > best) best = L.total;
+    }
+    return best;
+}
+
+hta_status hta_prefix_attn(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k_cache,
+                           const hta_bf16 *v_cache, const int32_t *cache_lens, float *o_c,
+                           float *lse_c, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_err, cudaStream_t stream) {
+    hta_status s = check_dims(d);
+    if (s != HTA_OK) return s;
+    if (!q || !k_cache || !v_cache || !cache_lens || !o_c || !lse_c) return HTA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_c)) return HTA_ERR_ALIGN;
+    return run_attention(d, q, k_cache, v_cache, cache_lens, nullptr, nullptr, nullptr, o_c, lse_c,
+                         true, true, false, workspace, workspace_bytes, dev_err, stream);
+}
+
+hta_status hta_tree_attn(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k_spec,
+                         const hta_bf16 *v_spec, const uint32_t *mask, float *o_s, float *lse_s,
+                         cudaStream_t stream) {
+    hta_status s = check_dims(d);
+    if (s != HTA_OK) return s;
+    if (!q || !k_spec || !v_spec || !mask || !o_s || !lse_s) return HTA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_spec) || !aligned16(v_spec) || !aligned16(o_s)) return HTA_ERR_ALIGN;
+    // the tree pass is a few MFLOP per head: it always takes the CUDA-core kernel
+    hta_dims dd = *d;
+    const int gmax = max_grid(kPathCC, &dd);
+    if (gmax <= 0) return HTA_ERR_CUDA;
+    Layout L = make_layout(&dd, kPathCC, 0, true);
+    AttnParams p = base_params(&dd, L);
+    p.q = (const __nv_bfloat16 *)q;
+    p.k_spec = (const __nv_bfloat16 *)k_spec;
+    p.v_spec = (const __nv_bfloat16 *)v_spec;
+    p.mask = mask;
+    p.out_o = o_s;
+    p.out_lse = lse_s;
+    p.out_fp32 = 1;
+    p.include_cache = 0;
+    p.include_tree = 1;
+    const int grid = (int)(L.n_seg < (int64_t)gmax ? L.n_seg : gmax);
+    if (hta::cc_launch(p, true, grid, stream) != cudaSuccess) return HTA_ERR_CUDA;
+    g_last_path = kPathCC;
+    return HTA_OK;
+}
+
+hta_status hta_merge(const hta_dims *d, const float *o_c, const float *lse_c, const float *o_s,
+                     const float *lse_s, hta_bf16 *o, float *lse, cudaStream_t stream) {
+    hta_status s = check_dims(d);
+    if (s != HTA_OK) return s;
+    if (!o_c || !lse_c || !o_s || !lse_s || !o || !lse) return HTA_ERR_INVALID_ARG;
+    if (!aligned16(o_c) || !aligned16(o_s) || !aligned16(o)) return HTA_ERR_ALIGN;
+    const int64_t rows = (int64_t)d->B * d->T * d->Hq;
+    if (hta::merge2_launch(rows, d->d, o_c, lse_c, o_s, lse_s, (__nv_bfloat16 *)o, lse, stream) !=
+        cudaSuccess)
+        return HTA_ERR_CUDA;
+    return HTA_OK;
+}
+
+hta_status hta_verify(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k_cache,
+                      const hta_bf16 *v_cache, const int32_t *cache_lens, const hta_bf16 *k_spec,
+                      const hta_bf16 *v_spec, const uint32_t *mask, hta_bf16 *o, float *lse,
+                      void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                      cudaStream_t stream) {
+    hta_status s = check_dims(d);
+    if (s != HTA_OK) return s;
+    if (!q || !k_cache || !v_cache || !cache_lens || !k_spec || !v_spec || !mask || !o || !lse)
+        return HTA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_spec) ||
+        !aligned16(v_spec) || !aligned16(o))
+        return HTA_ERR_ALIGN;
+    return run_attention(d, q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, o, lse, false,
+                         true, true, workspace, workspace_bytes, dev_err, stream);
+}
+
+}  // extern "C"

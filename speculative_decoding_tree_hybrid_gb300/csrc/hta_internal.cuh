@@ -1,0 +1,342 @@
+// Internal definitions shared by the libhta kernels: launch parameters, the
+// static split-KV schedule, the grid barrier and the cross-split /
+// cross-part log-sum-exp merge.
+//
+// Work decomposition (both kernel paths):
+//   segment s = ((b * Hkv) + kvh) * n_rg + rg : one KV head of one sequence and
+//               one group of its packed query rows (packed row r = t*G + g, so
+//               all G query heads of a KV head share every K/V tile);
+//   unit      = one tile of `tile` keys: tree tiles first (masked), then the
+//               cache tiles of that segment (unmasked, keys j < L_b);
+//   CTA c of the persistent grid owns units [c*U/grid, (c+1)*U/grid) of the
+//   linearised unit space, so every CTA gets the same number of tiles
+//   whatever the mix of cache lengths; a CTA whose range crosses a segment
+//   boundary emits one partial per segment piece.
+//   Piece (s, c) writes its partial (running max m in log2 units, denominator
+//   l, un-normalised O) to slot s + c; a monotone staircase of pieces makes
+//   that index unique.
+// After a grid-wide barrier every CTA merges a slice of all output rows over
+// the pieces of their segment: the log-sum-exp merge of the method ("LongSpec:
+// Long-Context Lossless Speculative Decoding with Efficient Drafting and
+// Verification", Korean summary section 2.C "aggregation").
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hta.h"
+
+namespace hta {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxSchedB = HTA_BMAX;
+
+struct AttnParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_cache;
+    const __nv_bfloat16 *v_cache;
+    const int32_t *cache_lens;
+    const __nv_bfloat16 *k_spec;
+    const __nv_bfloat16 *v_spec;
+    const uint32_t *mask;
+    void *out_o;     // bf16 or fp32 [B][T][Hq][d]
+    float *out_lse;  // fp32 [B][T][Hq]
+    int32_t out_fp32;
+    int32_t B, T, Hq, Hkv, G, d, W;
+    int64_t Lmax;
+    float scale_log2;  // softmax scale * log2(e)
+    int32_t R;         // packed rows per KV head = T * G
+    int32_t n_rg;      // row groups per KV head
+    int32_t rows_pg;   // rows per group (last group may be shorter)
+    int32_t include_cache, include_tree;
+    int32_t tile;          // keys per unit
+    int32_t n_tree_tiles;  // ceil(T / tile) when include_tree
+    // workspace
+    float *ws_o;  // [slots][rows_pg][d]
+    float *ws_m;  // [slots][rows_pg]
+    float *ws_l;  // [slots][rows_pg]
+    unsigned int *bar;  // [0] arrivals, [1] departures
+    int64_t slots;
+    int32_t *dev_err;
+};
+
+// ---------------------------------------------------------------- errors
+
+__device__ __forceinline__ void flag_error(int32_t *dev_err, int32_t f) {
+    if (dev_err) atomicOr(dev_err, f);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- schedule
+
+// Units of one segment of sequence b.
+__device__ __forceinline__ int32_t seg_units(const AttnParams &p, int32_t Lb) {
+    int32_t u = p.include_tree ? p.n_tree_tiles : 0;
+    if (p.include_cache) u += (Lb + p.tile - 1) / p.tile;
+    return u;
+}
+
+__device__ __forceinline__ int32_t clamp_len(const AttnParams &p, int32_t L) {
+    if (L < 0 || (int64_t)L > p.Lmax) {
+        flag_error(p.dev_err, HTA_DEVERR_CACHE_LEN);
+        L = L < 0 ? 0 : (int32_t)p.Lmax;
+    }
+    return L;
+}
+
+// Builds, in shared memory, the clamped lengths lens_s[b] and the exclusive
+// prefix pre_s[b] = sum_{b' < b} Hkv * n_rg * seg_units(b'); pre_s[B] = U.
+// Must be called by every thread of the block. Reports bad lengths once (CTA 0).
+__device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int64_t *pre_s,
+                                      int64_t *scratch /* [blockDim.x] */) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (p.B + nt - 1) / nt;
+    const int b0 = tid * per;
+    int64_t local = 0;
+    for (int b = b0; b < b0 + per && b < p.B; ++b) {
+        int32_t L = p.cache_lens[b];
+        if (L < 0 || (int64_t)L > p.Lmax) {
+            if (blockIdx.x == 0) flag_error(p.dev_err, HTA_DEVERR_CACHE_LEN);
+            L = L < 0 ? 0 : (int32_t)p.Lmax;
+        }
+        lens_s[b] = L;
+        local += (int64_t)p.Hkv * p.n_rg * seg_units(p, L);
+    }
+    scratch[tid] = local;
+    __syncthreads();
+    if (tid == 0) {
+        int64_t run = 0;
+        for (int i = 0; i < nt; ++i) {
+            int64_t v = scratch[i];
+            scratch[i] = run;
+            run += v;
+        }
+        pre_s[p.B] = run;
+    }
+    __syncthreads();
+    int64_t run = scratch[tid];
+    for (int b = b0; b < b0 + per && b < p.B; ++b) {
+        pre_s[b] = run;
+        run += (int64_t)p.Hkv * p.n_rg * seg_units(p, lens_s[b]);
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ int64_t cta_lo(int64_t c, int64_t U, int64_t grid) {
+    return (c * U) / grid;
+}
+
+// CTA that owns unit u (the unique c with lo(c) <= u < lo(c+1)).
+__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t grid) {
+    int64_t c = (u * grid) / U;
+    if (c >= grid) c = grid - 1;
+    while (c + 1 < grid && cta_lo(c + 1, U, grid) <= u) ++c;
+    while (c > 0 && cta_lo(c, U, grid) > u) --c;
+    return c;
+}
+
+// Sequence containing unit u: largest b with pre_s[b] <= u (binary search).
+__device__ __forceinline__ int32_t seq_of_unit(int64_t u, const int64_t *pre_s, int32_t B) {
+    int32_t lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int32_t mid = (lo + hi + 1) >> 1;
+        if (pre_s[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct UnitPos {
+    int32_t b, kvh, rg;
+    int64_t seg;         // segment index
+    int32_t unit;        // unit index inside the segment
+    int32_t seg_units;   // units in the segment
+    int64_t seg_begin;   // first global unit of the segment
+};
+
+__device__ __forceinline__ UnitPos locate_unit(const AttnParams &p, int64_t u, const int32_t *lens_s,
+                                               const int64_t *pre_s) {
+    UnitPos r;
+    r.b = seq_of_unit(u, pre_s, p.B);
+    // skip sequences with zero units (several b may share pre_s)
+    r.seg_units = seg_units(p, lens_s[r.b]);
+    const int64_t off = u - pre_s[r.b];
+    const int64_t sl = off / r.seg_units;
+    r.unit = (int32_t)(off - sl * r.seg_units);
+    r.kvh = (int32_t)(sl / p.n_rg);
+    r.rg = (int32_t)(sl - (int64_t)r.kvh * p.n_rg);
+    r.seg = ((int64_t)r.b * p.Hkv + r.kvh) * p.n_rg + r.rg;
+    r.seg_begin = pre_s[r.b] + sl * r.seg_units;
+    return r;
+}
+
+__device__ __forceinline__ int32_t rows_in_group(const AttnParams &p, int32_t rg) {
+    int32_t r0 = rg * p.rows_pg;
+    int32_t n = p.R - r0;
+    return n < p.rows_pg ? n : p.rows_pg;
+}
+
+// ---------------------------------------------------------------- barrier
+
+// Grid-wide barrier for a cooperative launch (every CTA is resident). The
+// wait is bounded by ~2 s of device time; on expiry the error flag is set and
+// the barrier reports failure instead of hanging. Every call returns the two
+// counters to zero once the last CTA has left.
+__device__ inline bool grid_barrier(const AttnParams &p) {
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(&p.bar[0], 1u);
+        const uint64_t t0 = globaltimer_ns();
+        int ok = 1;
+        unsigned int v;
+        for (;;) {
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.bar) : "memory");
+            if (v >= gridDim.x) break;
+            if (globaltimer_ns() - t0 > 2000000000ull) {
+                ok = 0;
+                flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        ok_s = ok;
+    }
+    __syncthreads();
+    return ok_s != 0;
+}
+
+// Called once per CTA after its last read of data published before the
+// barrier; the last CTA out resets both counters for the next call.
+__device__ inline void grid_barrier_depart(const AttnParams &p) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned int old = atomicAdd(&p.bar[1], 1u);
+        if (old == gridDim.x - 1) {
+            atomicExch(&p.bar[0], 0u);
+            atomicExch(&p.bar[1], 0u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- partials
+
+__device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return seg + cta; }
+
+// ---------------------------------------------------------------- merge phase
+
+// Merges every output row handled by this CTA: rows are the packed rows of
+// all segments, linearised segment-major and split evenly over the grid.
+// One warp per row. Lane k first reads the running max and denominator of
+// piece k (32 pieces at a time) so the loads overlap; the weights are then
+// broadcast and each lane accumulates d/32 adjacent columns.
+template <int D>
+__device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
+                                   bool barrier_ok) {
+    constexpr int CPL = D / 32;  // columns per lane
+    const int64_t n_seg = (int64_t)p.B * p.Hkv * p.n_rg;
+    const int64_t rows_total = n_seg * p.rows_pg;  // includes padding rows of short groups
+    const int64_t grid = gridDim.x;
+    const int64_t r0 = (blockIdx.x * rows_total) / grid;
+    const int64_t r1 = ((blockIdx.x + 1) * rows_total) / grid;
+    const int64_t U = pre_s[p.B];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int64_t rr = r0 + warp; rr < r1; rr += nwarps) {
+        const int64_t seg = rr / p.rows_pg;
+        const int32_t lr = (int32_t)(rr - seg * p.rows_pg);
+        const int32_t rg = (int32_t)(seg % p.n_rg);
+        const int32_t kvh = (int32_t)((seg / p.n_rg) % p.Hkv);
+        const int32_t b = (int32_t)(seg / ((int64_t)p.n_rg * p.Hkv));
+        if (lr >= rows_in_group(p, rg)) continue;
+        const int32_t r = rg * p.rows_pg + lr;  // packed row
+        const int32_t t = r / p.G, hq = kvh * p.G + (r - t * p.G);
+        const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
+
+        const int32_t su = seg_units(p, lens_s[b]);
+        const int64_t sb = pre_s[b] + ((int64_t)kvh * p.n_rg + rg) * su;
+        int64_t c_first = 0, n_pieces = 0;
+        if (su > 0 && barrier_ok) {
+            c_first = cta_of_unit(sb, U, grid);
+            n_pieces = cta_of_unit(sb + su - 1, U, grid) - c_first + 1;
+        }
+        // pass 1: global max over pieces
+        float M = -INFINITY;
+        for (int64_t k0 = 0; k0 < n_pieces; k0 += 32) {
+            const int64_t c = c_first + k0 + lane;
+            float m = -INFINITY;
+            if (k0 + lane < n_pieces && cta_lo(c, U, grid) != cta_lo(c + 1, U, grid))
+                m = p.ws_m[slot_of(seg, c) * p.rows_pg + lr];
+            M = fmaxf(M, m);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        // pass 2: weights, denominator, weighted sum of the un-normalised outputs
+        float den = 0.f;
+        float acc[CPL];
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
+        if (M > -INFINITY) {
+            for (int64_t k0 = 0; k0 < n_pieces; k0 += 32) {
+                const int64_t c = c_first + k0 + lane;
+                float w = 0.f;
+                if (k0 + lane < n_pieces && cta_lo(c, U, grid) != cta_lo(c + 1, U, grid)) {
+                    const int64_t sidx = slot_of(seg, c) * p.rows_pg + lr;
+                    const float m = p.ws_m[sidx];
+                    if (m > -INFINITY) {
+                        w = exp2f(m - M);
+                        den += w * p.ws_l[sidx];
+                    }
+                }
+                const int nk = (int)((n_pieces - k0) < 32 ? (n_pieces - k0) : 32);
+                for (int k = 0; k < nk; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w, k);
+                    if (wk == 0.f) continue;
+                    const int64_t sidx = slot_of(seg, c_first + k0 + k) * p.rows_pg + lr;
+                    const float *o = p.ws_o + sidx * D + lane * CPL;
+                    if constexpr (CPL == 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(o);
+                        acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2 *>(o);
+                        acc[0] += wk * v.x; acc[1] += wk * v.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        }
+        float lse, inv;
+        if (!barrier_ok) {
+            lse = __int_as_float(0x7fc00000);
+            inv = __int_as_float(0x7fc00000);
+        } else if (den > 0.f) {
+            lse = (M + log2f(den)) * kLn2;
+            inv = 1.f / den;
+        } else {
+            lse = -INFINITY;  // no visible key: empty softmax
+            inv = 0.f;
+        }
+        if (p.out_fp32) {
+            float *o = (float *)p.out_o + out_row * D + lane * CPL;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) o[k] = acc[k] * inv;
+        } else {
+            __nv_bfloat16 *o = (__nv_bfloat16 *)p.out_o + out_row * D + lane * CPL;
+#pragma unroll
+            for (int k = 0; k < CPL; k += 2)
+                *reinterpret_cast<__nv_bfloat162 *>(o + k) =
+                    __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+        }
+        if (lane == 0) p.out_lse[out_row] = lse;
+    }
+}
+
+}  // namespace hta

@@ -1,0 +1,30 @@
+// Host-side launch interface between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "hta_internal.cuh"
+
+namespace hta {
+
+// CUDA-core path (k_cc.cu)
+int cc_rows_per_group();
+int cc_tile();
+int cc_max_grid(int d, int B, int num_sms);
+cudaError_t cc_launch(const AttnParams &p, bool direct, int grid, cudaStream_t stream);
+
+// tcgen05 path (k_tc.cu)
+int tc_rows_per_group();
+int tc_tile();
+int tc_max_grid(int B, int num_sms);
+cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream);
+
+// tree mask (k_mask.cu)
+cudaError_t mask_launch(const int32_t *parents, int B, int T, uint32_t *mask, int32_t *dev_err,
+                        cudaStream_t stream);
+
+// two-part merge (k_merge.cu)
+cudaError_t merge2_launch(int64_t rows, int d, const float *o_c, const float *lse_c, const float *o_s,
+                          const float *lse_s, __nv_bfloat16 *o, float *lse, cudaStream_t stream);
+
+}  // namespace hta

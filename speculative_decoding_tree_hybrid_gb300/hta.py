@@ -1,0 +1,263 @@
+"""Thin ctypes binding of libhta (C ABI declared in include/hta.h).
+
+Argument marshalling only: every function checks tensor devices, dtypes and
+shapes, allocates outputs through torch, and passes raw device pointers and
+torch's current CUDA stream to the library. All computation happens in the
+library's CUDA kernels; there is no fallback of any kind, and loading fails
+loudly when libhta.so has not been built.
+
+bf16 tensors are torch.bfloat16; masks are int32 tensors holding the uint32
+mask words bit for bit.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+_ws_cache: dict = {}
+
+PATH_CC, PATH_TC = 1, 2
+DEVERR_BAD_TREE, DEVERR_CACHE_LEN, DEVERR_TIMEOUT = 1, 2, 4
+TMAX, BMAX = 256, 1024
+
+# every exported symbol of include/hta.h
+EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
+           "hta_merge", "hta_verify", "hta_status_string", "hta_last_path")
+
+
+class HtaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class HtaDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("Lmax", ctypes.c_int64),
+                ("scale", ctypes.c_float)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Loads libhta.so from the package's build folder (raises if absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libhta.so is not built ({path}); call "
+                               "speculative_decoding_tree_hybrid_gb300.build.build() first")
+        lib = ctypes.CDLL(path)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        D = ctypes.POINTER(HtaDims)
+        lib.hta_build_mask.argtypes = [P, I32, I32, P, P, P]
+        lib.hta_workspace_bytes.argtypes = [D]
+        lib.hta_workspace_bytes.restype = SZ
+        lib.hta_prefix_attn.argtypes = [D, P, P, P, P, P, P, P, SZ, P, P]
+        lib.hta_tree_attn.argtypes = [D, P, P, P, P, P, P, P]
+        lib.hta_merge.argtypes = [D, P, P, P, P, P, P, P]
+        lib.hta_verify.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+        lib.hta_status_string.argtypes = [ctypes.c_int]
+        lib.hta_status_string.restype = ctypes.c_char_p
+        lib.hta_last_path.restype = I32
+        for name in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge", "hta_verify"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().hta_status_string(int(status)).decode()
+
+
+def last_path() -> int:
+    return int(load().hta_last_path())
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def dims_of(q, k_cache, scale: float = 0.0) -> HtaDims:
+    B, T, Hq, d = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    return HtaDims(B, T, Hq, Hkv, d, Lmax, float(scale))
+
+
+def workspace_bytes(dims: HtaDims) -> int:
+    return int(load().hta_workspace_bytes(ctypes.byref(dims)))
+
+
+def workspace(dims: HtaDims, device) -> torch.Tensor:
+    """A zero-initialised workspace for these dims, cached per device and stream.
+
+    Calls that share it must run in stream order (the library resets its
+    barrier counters at the end of every call).
+    """
+    device = torch.device(device)
+    nbytes = workspace_bytes(dims)
+    if nbytes == 0:
+        raise HtaError(-1, "hta_workspace_bytes")
+    key = (device, _stream(device))
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _raise(status: int, what: str):
+    if status != 0:
+        raise HtaError(status, what)
+
+
+def build_mask(parents: torch.Tensor, dev_err: torch.Tensor | None = None,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """parents int32 [B][T] -> ancestor-or-self mask words int32 [B][T][ceil(T/32)]."""
+    _check(parents, "parents", torch.int32, 2)
+    B, T = parents.shape
+    if out is None:
+        mask = torch.empty((B, T, (T + 31) // 32), dtype=torch.int32, device=parents.device)
+    else:
+        _check(out, "out", torch.int32, 3, parents.device)
+        if tuple(out.shape) != (B, T, (T + 31) // 32):
+            raise ValueError("out must be [B][T][ceil(T/32)]")
+        mask = out
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, parents.device)
+    with torch.cuda.device(parents.device):
+        _raise(load().hta_build_mask(_ptr(parents), B, T, _ptr(mask), _ptr(dev_err),
+                                     _stream(parents.device)), "hta_build_mask")
+    return mask
+
+
+def _check_qkv(q, k_cache, v_cache, cache_lens):
+    _check(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _check(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _check(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _check(cache_lens, "cache_lens", torch.int32, 1, dev)
+    B, T, Hq, d = q.shape
+    if k_cache.shape[0] != B or k_cache.shape[3] != d or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [B][Hkv][Lmax][d] matching q")
+    if cache_lens.shape[0] != B:
+        raise ValueError("cache_lens must be [B]")
+
+
+def _check_spec(q, k_spec, v_spec, mask, Hkv):
+    B, T, Hq, d = q.shape
+    dev = q.device
+    _check(k_spec, "k_spec", torch.bfloat16, 4, dev)
+    _check(v_spec, "v_spec", torch.bfloat16, 4, dev)
+    _check(mask, "mask", torch.int32, 3, dev)
+    if tuple(k_spec.shape) != (B, Hkv, T, d) or v_spec.shape != k_spec.shape:
+        raise ValueError("k_spec/v_spec must be [B][Hkv][T][d]")
+    if tuple(mask.shape) != (B, T, (T + 31) // 32):
+        raise ValueError("mask must be [B][T][ceil(T/32)]")
+
+
+def verify(q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, *, scale: float = 0.0,
+           ws: torch.Tensor | None = None, dev_err: torch.Tensor | None = None,
+           out: tuple | None = None):
+    """Fused hybrid tree attention. Returns (o bf16 [B][T][Hq][d], lse fp32 [B][T][Hq])."""
+    _check_qkv(q, k_cache, v_cache, cache_lens)
+    _check_spec(q, k_spec, v_spec, mask, k_cache.shape[1])
+    dims = dims_of(q, k_cache, scale)
+    dev = q.device
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    else:
+        o, lse = out
+    if ws is None:
+        ws = workspace(dims, dev)
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_verify(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(cache_lens), _ptr(k_spec), _ptr(v_spec), _ptr(mask), _ptr(o),
+                                 _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_err), _stream(dev)),
+               "hta_verify")
+    return o, lse
+
+
+def prefix_attn(q, k_cache, v_cache, cache_lens, *, scale: float = 0.0,
+                ws: torch.Tensor | None = None, dev_err: torch.Tensor | None = None):
+    """Cached part alone. Returns (o_c fp32 [B][T][Hq][d], lse_c fp32 [B][T][Hq])."""
+    _check_qkv(q, k_cache, v_cache, cache_lens)
+    dims = dims_of(q, k_cache, scale)
+    dev = q.device
+    o_c = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse_c = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(dims, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_prefix_attn(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(cache_lens), _ptr(o_c), _ptr(lse_c), _ptr(ws), ws.numel(),
+                                      _ptr(dev_err), _stream(dev)), "hta_prefix_attn")
+    return o_c, lse_c
+
+
+def tree_attn(q, k_spec, v_spec, mask, *, scale: float = 0.0):
+    """Speculative part alone. Returns (o_s fp32 [B][T][Hq][d], lse_s fp32 [B][T][Hq])."""
+    _check(q, "q", torch.bfloat16, 4)
+    Hkv = k_spec.shape[1]
+    _check_spec(q, k_spec, v_spec, mask, Hkv)
+    B, T, Hq, d = q.shape
+    dims = HtaDims(B, T, Hq, Hkv, d, 0, float(scale))
+    dev = q.device
+    o_s = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse_s = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_tree_attn(ctypes.byref(dims), _ptr(q), _ptr(k_spec), _ptr(v_spec),
+                                    _ptr(mask), _ptr(o_s), _ptr(lse_s), _stream(dev)), "hta_tree_attn")
+    return o_s, lse_s
+
+
+def merge(o_c, lse_c, o_s, lse_s):
+    """Log-sum-exp merge of two partial softmaxes. Returns (o bf16, lse fp32)."""
+    _check(o_c, "o_c", torch.float32, 4)
+    dev = o_c.device
+    _check(o_s, "o_s", torch.float32, 4, dev)
+    _check(lse_c, "lse_c", torch.float32, 3, dev)
+    _check(lse_s, "lse_s", torch.float32, 3, dev)
+    B, T, Hq, d = o_c.shape
+    if o_s.shape != o_c.shape or tuple(lse_c.shape) != (B, T, Hq) or lse_s.shape != lse_c.shape:
+        raise ValueError("partials must share [B][T][Hq][d] / [B][T][Hq]")
+    dims = HtaDims(B, T, Hq, 1, d, 0, 0.0)
+    o = torch.empty(o_c.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(lse_c.shape, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_merge(ctypes.byref(dims), _ptr(o_c), _ptr(lse_c), _ptr(o_s), _ptr(lse_s),
+                                _ptr(o), _ptr(lse), _stream(dev)), "hta_merge")
+    return o, lse

@@ -1,0 +1,97 @@
+"""CPU checks of the C-ABI boundary: the library builds for sm_103a, loads,
+exports every function include/hta.h declares, and rejects bad arguments on
+the host before any launch. No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_tree_hybrid_gb300 import build as hbuild
+from speculative_decoding_tree_hybrid_gb300 import hta
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "hta.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hbuild.build()
+    return hta.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hta_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for required in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge",
+                     "hta_verify", "hta_workspace_bytes", "hta_status_string"):
+        assert required in names
+    assert set(names) == set(hta.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = hta.status_string(code)
+        assert s and s != "unknown status"
+    assert hta.status_string(-99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(B=1, T=8, Hq=4, Hkv=1, d=64, Lmax=256, scale=0.0)
+    base.update(kw)
+    return hta.HtaDims(base["B"], base["T"], base["Hq"], base["Hkv"], base["d"], base["Lmax"], base["scale"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), -1), (dict(T=0), -1), (dict(Hq=0), -1), (dict(Lmax=-1), -1), (dict(scale=-1.0), -1),
+    (dict(Hq=6, Hkv=4), -2), (dict(d=96), -2), (dict(T=257), -2), (dict(B=1025), -2),
+])
+def test_verify_rejects_bad_dims_on_host(lib, kw, status):
+    d = _dims(**kw)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the call returns before any launch
+    st = lib.hta_verify(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                        1 << 20, None, None)
+    assert st == status
+
+
+def test_verify_rejects_null_and_misaligned_pointers(lib):
+    d = _dims()
+    good = ctypes.c_void_p(1 << 20)
+    args = [good] * 10
+    for i in range(9):
+        a = list(args)
+        a[i] = None
+        assert lib.hta_verify(ctypes.byref(d), *a, 1 << 20, None, None) == -1
+    a = list(args)
+    a[0] = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.hta_verify(ctypes.byref(d), *a, 1 << 20, None, None) == -3
+
+
+def test_build_mask_rejects_bad_sizes(lib):
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.hta_build_mask(None, 1, 8, p, None, None) == -1
+    assert lib.hta_build_mask(p, 0, 8, p, None, None) == -1
+    assert lib.hta_build_mask(p, 1, 257, p, None, None) == -2
+
+
+def test_merge_and_tree_reject_bad_args(lib):
+    d = _dims()
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.hta_merge(ctypes.byref(d), None, p, p, p, p, p, None) == -1
+    assert lib.hta_tree_attn(ctypes.byref(d), p, p, p, p, p, None, None) == -1
+    assert lib.hta_prefix_attn(None, p, p, p, p, p, p, p, 0, None, None) == -1
+
+
+def test_workspace_query_without_device_is_zero_or_sized(lib):
+    n = hta.workspace_bytes(_dims())
+    assert n == 0 or n >= 256
+    assert hta.workspace_bytes(_dims(d=96)) == 0
