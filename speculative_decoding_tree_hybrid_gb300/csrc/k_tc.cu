@@ -1,9 +1,575 @@
-// tcgen05 tensor-core path (placeholder until the kernel lands).
+// tcgen05 tensor-core path of the hybrid tree attention (head dimension 128).
+//
+// The method ("LongSpec: Long-Context Lossless Speculative Decoding with
+// Efficient Drafting and Verification", Korean summary section 2.C, Dutch
+// summary Methodologie section 3) splits the verification attention into an
+// unmasked pass over the long cached prefix and a masked pass over the tree
+// tokens, merged by log-sum-exp. Here both passes are 128-key tiles of one
+// persistent cooperative grid (one CTA per SM, a static split-KV schedule
+// balanced by tile count, see hta_internal.cuh), and the cross-split and
+// cross-part merge runs after a grid barrier in the same launch.
+//
+// One CTA works on a row group of up to 256 packed query rows of one KV head
+// (row r = t*G + g, so every K/V tile is shared by all G query heads of the
+// tree), as two 128-row halves:
+//   warp 0        TMA producer: K and V tiles (128 keys x 128 dims, bf16,
+//                 128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1        MMA issuer (one thread): S_h = Q_h K^T into tensor memory,
+//                 then O_h += P_h V with P_h read from tensor memory;
+//   warps 4-7     softmax of half 0, one query row per thread;
+//   warps 8-11    softmax of half 1.
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each; P_h
+// (bf16) overwrites the first 64 columns of S_h. The MMA order
+// PV(0,i), S(0,i+1), PV(1,i), S(1,i+1) lets the softmax of one half overlap
+// the other half's MMAs, and tensor-core operations of one thread execute in
+// issue order, so S(h,i+1) never overtakes PV(h,i) that still reads P_h.
+// The softmax keeps the row max in base 2 (scores times scale*log2 e) and
+// rescales O in tensor memory only when the max grows by more than 8
+// (factor 256), which leaves the result exact because numerator and
+// denominator share the stale max.
+//
+// Every wait is bounded (~1 s of device time); on expiry the kernel sets
+// HTA_DEVERR_TIMEOUT, waits for its own copies in flight, frees its tensor
+// memory and finishes instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "hta_launch.h"
+#include "tc_ptx.cuh"
 
 namespace hta {
-int tc_rows_per_group() { return 0; }
-int tc_tile() { return 128; }
-int tc_max_grid(int, int) { return 0; }
-cudaError_t tc_launch(const AttnParams &, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;          // keys per tile
+constexpr int kHalf = 128;          // query rows per MMA
+constexpr int kMaxRows = 256;       // rows per row group
+constexpr int kStages = 4;          // K/V ring stages
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one K or V tile
+constexpr uint32_t kSubBytes = 128 * 64 * 2;    // one 64-dim swizzled sub-tile
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffShared = kOffRing + kStages * kTileBytes;
+constexpr uint32_t kSharedBytes = 512;
+constexpr uint32_t kOffSched = kOffShared + kSharedBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct TcMaps {
+    CUtensorMap kc, vc, ks, vs;
+};
+
+struct TcShared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2], q_full[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+static_assert(sizeof(TcShared) <= kSharedBytes, "shared control block too large");
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_u32(&b); }
+
+// Bounded wait on an mbarrier phase; false on timeout or when another warp
+// has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort,
+                                         int32_t *dev_err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *abort = 1;
+            flag_error(dev_err, HTA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Walks the CTA's unit range tile by tile, piece by piece.
+struct Cursor {
+    int64_t u, u_end;
+    int32_t q;      // piece counter
+    int32_t left;   // tiles left in the current piece
+    int32_t unit;   // next unit index inside the segment
+    int32_t b, kvh, rg, Lb;
+    int64_t seg;
+};
+
+struct TileInfo {
+    int32_t q, unit, b, kvh, rg, Lb;
+    int64_t seg;
+    bool first, last;
+};
+
+__device__ __forceinline__ void cursor_init(Cursor &c, int64_t u0, int64_t u1) {
+    c.u = u0;
+    c.u_end = u1;
+    c.q = -1;
+    c.left = 0;
+    c.unit = 0;
+    c.b = c.kvh = c.rg = c.Lb = 0;
+    c.seg = 0;
+}
+
+__device__ __forceinline__ bool cursor_next(Cursor &c, const AttnParams &p, const int32_t *lens_s,
+                                            const int64_t *pre_s, TileInfo &t) {
+    t.first = false;
+    if (c.left == 0) {
+        if (c.u >= c.u_end) return false;
+        const UnitPos pos = locate_unit(p, c.u, lens_s, pre_s);
+        const int64_t seg_end = pos.seg_begin + pos.seg_units;
+        const int64_t piece_end = seg_end < c.u_end ? seg_end : c.u_end;
+        c.left = (int32_t)(piece_end - c.u);
+        c.unit = pos.unit;
+        c.b = pos.b;
+        c.kvh = pos.kvh;
+        c.rg = pos.rg;
+        c.seg = pos.seg;
+        c.Lb = lens_s[pos.b];
+        c.q += 1;
+        c.u = piece_end;
+        t.first = true;
+    }
+    t.q = c.q;
+    t.unit = c.unit;
+    t.b = c.b;
+    t.kvh = c.kvh;
+    t.rg = c.rg;
+    t.seg = c.seg;
+    t.Lb = c.Lb;
+    c.unit += 1;
+    c.left -= 1;
+    t.last = c.left == 0;
+    return true;
+}
+
+// ------------------------------------------------------------------ roles
+
+__device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, uint32_t ring,
+                         const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+    volatile int32_t *abort = &sh.abort;
+    const int n_tree = p.include_tree ? p.n_tree_tiles : 0;
+    Cursor c;
+    cursor_init(c, u0, u1);
+    TileInfo t;
+    uint32_t n = 0;  // ring fills issued
+    bool ok = true;
+    while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
+        const bool tree = t.unit < n_tree;
+        const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
+        const int z = t.b * p.Hkv + t.kvh;
+        for (int kv = 0; kv < 2; ++kv, ++n) {
+            const uint32_t st = n % kStages, round = n / kStages;
+            if (!wait_bar(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err)) {
+                ok = false;
+                break;
+            }
+            const CUtensorMap *map = tree ? (kv ? &maps.vs : &maps.ks) : (kv ? &maps.vc : &maps.kc);
+            const uint32_t full = bar_addr(sh.full[st]);
+            mbar_arrive_expect_tx(full, kTileBytes);
+            tma_load_3d(ring + st * kTileBytes, map, full, 0, y, z);
+            tma_load_3d(ring + st * kTileBytes + kSubBytes, map, full, 64, y, z);
+        }
+    }
+    if (!ok) {
+        // let the copies already issued land before the CTA exits
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t k = n > (uint32_t)kStages ? n - kStages : 0; k < n; ++k) {
+            const uint32_t st = k % kStages, round = k / kStages;
+            while (!mbar_try_wait(bar_addr(sh.full[st]), round & 1))
+                if (globaltimer_ns() - t0 > kTimeoutNs) break;
+        }
+    }
+}
+
+__device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
+                           int halves, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+    volatile int32_t *abort = &sh.abort;
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
+    Cursor c;
+    cursor_init(c, u0, u1);
+    TileInfo cur, nxt;
+    bool has_cur = cursor_next(c, p, lens_s, pre_s, cur);
+    if (!has_cur) return;
+
+    // S_h(i) = Q_h K(i)^T
+    auto issue_s = [&](int h, uint32_t i, const TileInfo &ti) -> bool {
+        const uint32_t n = 2 * i, st = n % kStages, round = n / kStages;
+        if (h == 0 && !wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return false;
+        if (ti.first && !wait_bar(bar_addr(sh.q_full[h]), ti.q & 1, abort, p.dev_err)) return false;
+        tc_fence_after();
+        const uint32_t qa = sQ + h * kTileBytes, kb = ring + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+            mma_ss(tmem + kColS + h * 128, smem_desc_sw128(qa + off, 16, 1024),
+                   smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
+        }
+        mma_commit(bar_addr(sh.s_full[h]));
+        if (h == halves - 1) mma_commit(bar_addr(sh.empty[st]));
+        return true;
+    };
+
+    for (int h = 0; h < halves; ++h)
+        if (!issue_s(h, 0, cur)) return;
+    for (uint32_t i = 0;; ++i) {
+        const bool has_next = cursor_next(c, p, lens_s, pre_s, nxt);
+        const uint32_t n = 2 * i + 1, st = n % kStages, round = n / kStages;
+        if (!wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return;
+        const uint32_t vb = ring + st * kTileBytes;
+        for (int h = 0; h < halves; ++h) {
+            if (!wait_bar(bar_addr(sh.p_full[h]), i & 1, abort, p.dev_err)) return;
+            if (cur.first && cur.q > 0 &&
+                !wait_bar(bar_addr(sh.o_free[h]), (cur.q - 1) & 1, abort, p.dev_err))
+                return;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tmem + kColO + h * 128, tmem + kColS + h * 128 + kk * 8,
+                       smem_desc_sw128(vb + kk * 2048, kSubBytes, 1024), idesc_pv,
+                       (!cur.first || kk > 0) ? 1u : 0u);
+            if (h == halves - 1) mma_commit(bar_addr(sh.empty[st]));
+            if (cur.last) mma_commit(bar_addr(sh.o_done[h]));
+            if (has_next && !issue_s(h, i + 1, nxt)) return;
+        }
+        if (!has_next) break;
+        cur = nxt;
+    }
+}
+
+__device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
+                           int h, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+    volatile int32_t *abort = &sh.abort;
+    const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
+    const int row = wq * 32 + lane;  // row of this half == TMEM lane
+    const int tid_wg = threadIdx.x & 127;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS + h * 128;
+    const uint32_t tO = tmem + lane_off + kColO + h * 128;
+    const int n_tree = p.include_tree ? p.n_tree_tiles : 0;
+    const float c2 = p.scale_log2;
+
+    Cursor c;
+    cursor_init(c, u0, u1);
+    TileInfo t;
+    uint32_t gi = 0;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool o_valid = false, valid = false;
+    int r_local = 0;
+    uint32_t mw[HTA_TMAX / 32];
+
+    while (cursor_next(c, p, lens_s, pre_s, t)) {
+        if (t.first) {
+            const int nrows = rows_in_group(p, t.rg);
+            r_local = h * kHalf + row;
+            valid = r_local < nrows;
+            const int r = t.rg * p.rows_pg + r_local;
+            const int tn = valid ? r / p.G : 0;
+            const int hq = t.kvh * p.G + (r - tn * p.G);
+            // this row of Q_h, 128-byte swizzled, zero for padding rows
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + (((int64_t)t.b * p.T + tn) * p.Hq + hq) * 128);
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint4 v = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+                const uint32_t dst = sQ + h * kTileBytes + (ch >> 3) * kSubBytes + row * 128 +
+                                     (((ch & 7) ^ (row & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                             "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_addr(sh.q_full[h]));
+            if (p.include_tree) {
+#pragma unroll
+                for (int w = 0; w < HTA_TMAX / 32; ++w)
+                    mw[w] = (valid && w < p.W) ? __ldg(p.mask + ((int64_t)t.b * p.T + tn) * p.W + w) : 0u;
+            }
+            m_run = -INFINITY;
+            l_run = 0.f;
+            o_valid = false;
+        }
+        const bool tree = t.unit < n_tree;
+        const int j0 = (tree ? t.unit : t.unit - n_tree) * kTile;
+        const int nvalid = tree ? min(kTile, p.T - j0) : min(kTile, t.Lb - j0);
+
+        bool ok = wait_bar(bar_addr(sh.s_full[h]), gi & 1, abort, p.dev_err);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld32(tS + 32 * k, s[k]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) reg_fence32(s[k]);
+
+        // mask words of this tile (a tree has at most two tiles of 128 keys);
+        // rows past the group see every key (their result is discarded)
+        uint32_t w4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w4[k] = (tree && valid) ? (t.unit == 0 ? mw[k] : mw[4 + k]) : 0xffffffffu;
+        // scaled scores (base 2), masked keys -inf
+        float m_tile = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int col = 32 * k + e;
+                const bool vis = col < nvalid && ((w4[k] >> e) & 1u);
+                const float x = vis ? __uint_as_float(s[k][e]) * c2 : -INFINITY;
+                s[k][e] = __float_as_uint(x);
+                m_tile = fmaxf(m_tile, x);
+            }
+        }
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool need = m_new > m_run + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+            alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+        }
+        if (__any_sync(0xffffffffu, need && o_valid)) {
+            const float a = (need && o_valid) ? alpha : 1.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * k, o);
+                tmem_wait_ld();
+                reg_fence32(o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
+                tmem_st32(tO + 32 * k, o);
+            }
+            tmem_wait_st();
+        }
+        // a partial last cache tile: clear the V rows past the sequence end
+        // (they may hold anything, and 0 * NaN would poison O)
+        if (h == 0 && !tree && nvalid < kTile) {
+            const uint32_t n = 2 * gi + 1, st = n % kStages, round = n / kStages;
+            ok = wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const uint32_t vb = ring + st * kTileBytes;
+            const int chunks = (kTile - nvalid) * 8;  // 16-byte chunks per sub-tile
+            for (int ch = tid_wg; ch < 2 * chunks; ch += 128) {
+                const int sub = ch / chunks, k = ch - sub * chunks;
+                const uint32_t dst = vb + sub * kSubBytes + nvalid * 128 + k * 16;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+            }
+            fence_proxy_async_smem();
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2(__uint_as_float(s[2 * k2 + (e >> 4)][(e & 15) * 2]) - m_use);
+                const float p1 = ex2(__uint_as_float(s[2 * k2 + (e >> 4)][(e & 15) * 2 + 1]) - m_use);
+                lsum += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS + 32 * k2, pk);
+        }
+        l_run += lsum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_addr(sh.p_full[h]));
+        o_valid = true;
+
+        if (t.last) {
+            ok = wait_bar(bar_addr(sh.o_done[h]), t.q & 1, abort, p.dev_err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int64_t sidx = slot_of(t.seg, blockIdx.x) * p.rows_pg + r_local;
+            float *dst = p.ws_o + sidx * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * k, o);
+                tmem_wait_ld();
+                reg_fence32(o);
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<uint4 *>(dst + 32 * k + e) = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                }
+            }
+            if (valid) {
+                p.ws_m[sidx] = m_run;
+                p.ws_l[sidx] = l_run;
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(sh.o_free[h]));
+        }
+        ++gi;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_verify(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    TcShared &sh = *reinterpret_cast<TcShared *>(smem + kOffShared);
+    int32_t *lens_s = reinterpret_cast<int32_t *>(smem + kOffSched);
+    int64_t *pre_s = reinterpret_cast<int64_t *>(smem + kOffSched + ((p.B * 4 + 15) / 16) * 16);
+    int64_t *scratch = pre_s + p.B + 1;
+    const uint32_t sQ = smem_u32(smem + kOffQ), ring = smem_u32(smem + kOffRing);
+    const int warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_addr(sh.full[s]), 1);
+            mbar_init(bar_addr(sh.empty[s]), 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar_addr(sh.s_full[h]), 1);
+            mbar_init(bar_addr(sh.p_full[h]), 128);
+            mbar_init(bar_addr(sh.o_done[h]), 1);
+            mbar_init(bar_addr(sh.o_free[h]), 128);
+            mbar_init(bar_addr(sh.q_full[h]), 128);
+        }
+        mbar_init(bar_addr(sh.drain), 1);
+        sh.abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && (threadIdx.x & 31) == 0) {
+        tma_prefetch_desc(&maps.kc);
+        tma_prefetch_desc(&maps.vc);
+        if (p.include_tree) {
+            tma_prefetch_desc(&maps.ks);
+            tma_prefetch_desc(&maps.vs);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    build_schedule(p, lens_s, pre_s, scratch);  // ends with __syncthreads
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const int64_t U = pre_s[p.B];
+    const int64_t u0 = cta_lo(blockIdx.x, U, gridDim.x), u1 = cta_lo(blockIdx.x + 1, U, gridDim.x);
+    const int halves = (p.rows_pg + kHalf - 1) / kHalf;
+
+    // register split: 128 x 72 for the control warpgroup, 256 x 216 for the
+    // softmax warpgroups (= 384 x 168 at launch); restored before the merge
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+        if (warp == 0) {
+            if ((threadIdx.x & 31) == 0) producer(p, maps, sh, ring, lens_s, pre_s, u0, u1);
+        } else if (warp == 1) {
+            if ((threadIdx.x & 31) == 0) mma_issuer(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
+        }
+        __syncwarp();
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
+        const int h = (warp >> 2) - 1;
+        if (h < halves) softmax_wg(p, sh, sQ, ring, tmem, h, lens_s, pre_s, u0, u1);
+        __syncwarp();
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 168;");
+    }
+    __syncthreads();
+    if (warp < 4) asm volatile("setmaxnreg.inc.sync.aligned.u32 168;");
+    if (warp == 1) {
+        if ((threadIdx.x & 31) == 0) {
+            // every MMA of this CTA has finished before tensor memory is freed
+            mma_commit(bar_addr(sh.drain));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar_addr(sh.drain), 0))
+                if (globaltimer_ns() - t0 > kTimeoutNs) break;
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    const bool ok = grid_barrier(p);
+    merge_phase<128>(p, lens_s, pre_s, ok);
+    grid_barrier_depart(p);
+}
+
+size_t tc_smem_bytes(int B) {
+    return 1024 + kOffSched + ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8 + kThreads * 8;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// [rows][d=128] bf16 per (b, kv head), boxes of 128 rows x 64 dims, 128-byte swizzle
+bool encode_kv(CUtensorMap *map, const void *base, int64_t rows, int64_t heads) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)heads};
+    const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)(rows > 0 ? rows : 1) * 128 * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int tc_rows_per_group() { return kMaxRows; }
+int tc_tile() { return kTile; }
+
+int tc_max_grid(int B, int num_sms) {
+    const size_t smem = tc_smem_bytes(B);
+    if (cudaFuncSetAttribute(k_tc_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 0;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_tc_verify, kThreads, smem) != cudaSuccess)
+        return 0;
+    return occ * num_sms;
+}
+
+cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
+    TcMaps maps;
+    memset(&maps, 0, sizeof maps);
+    const int64_t heads = (int64_t)p.B * p.Hkv;
+    if (!encode_kv(&maps.kc, p.k_cache, p.Lmax, heads) || !encode_kv(&maps.vc, p.v_cache, p.Lmax, heads))
+        return cudaErrorInvalidValue;
+    if (p.include_tree &&
+        (!encode_kv(&maps.ks, p.k_spec, p.T, heads) || !encode_kv(&maps.vs, p.v_spec, p.T, heads)))
+        return cudaErrorInvalidValue;
+    const size_t smem = tc_smem_bytes(p.B);
+    cudaError_t e = cudaFuncSetAttribute(k_tc_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_tc_verify, p, maps);
+}
+
 }  // namespace hta

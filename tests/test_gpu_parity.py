@@ -231,7 +231,7 @@ def sample_rows(cfg, n, seed):
     rng = np.random.default_rng(seed)
     total = cfg.B * cfg.T * cfg.Hq
     corners = [0, cfg.Hq - 1, total - 1, total - cfg.Hq, (cfg.T // 2) * cfg.Hq + cfg.Hq // 2]
-    rows = np.unique(np.concatenate([rng.choice(total, size=n, replace=False), corners]))
+    rows = np.unique(np.concatenate([rng.choice(total, size=min(n, total), replace=False), corners]))
     return rows.astype(np.int64)
 
 
