@@ -72,7 +72,7 @@ int choose_path(const hta_dims *d) {
 struct Layout {
     int n_rg, rows_pg, tile, n_tree_tiles;
     int64_t n_seg, slots;
-    size_t off_m, off_l, off_o, total;
+    size_t off_rec, total;
 };
 
 Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
@@ -85,14 +85,9 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
     L.n_tree_tiles = tree ? (d->T + L.tile - 1) / L.tile : 0;
     L.n_seg = (int64_t)d->B * d->Hkv * L.n_rg;
     L.slots = L.n_seg + grid;
-    size_t off = kWsAlign;  // barrier counters
-    L.off_m = off;
-    off = align_up(off + (size_t)L.slots * L.rows_pg * sizeof(float), kWsAlign);
-    L.off_l = off;
-    off = align_up(off + (size_t)L.slots * L.rows_pg * sizeof(float), kWsAlign);
-    L.off_o = off;
-    off = align_up(off + (size_t)L.slots * L.rows_pg * d->d * sizeof(float), kWsAlign);
-    L.total = off;
+    // [barrier counters | partial records (d + 4 floats per row)]
+    L.off_rec = kWsAlign;
+    L.total = align_up(L.off_rec + (size_t)L.slots * L.rows_pg * (d->d + 4) * sizeof(float), kWsAlign);
     return L;
 }
 
@@ -160,9 +155,7 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
         if (!ws || ((uintptr_t)ws % kWsAlign) != 0 || ws_bytes < L.total) return HTA_ERR_WORKSPACE;
         char *base = (char *)ws;
         p.bar = (unsigned int *)base;
-        p.ws_m = (float *)(base + L.off_m);
-        p.ws_l = (float *)(base + L.off_l);
-        p.ws_o = (float *)(base + L.off_o);
+        p.ws_rec = (float *)(base + L.off_rec);
         p.slots = L.slots;
     }
     cudaError_t e;

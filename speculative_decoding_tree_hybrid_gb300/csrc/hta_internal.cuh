@@ -12,13 +12,16 @@
 //   linearised unit space, so every CTA gets the same number of tiles
 //   whatever the mix of cache lengths; a CTA whose range crosses a segment
 //   boundary emits one partial per segment piece.
-//   Piece (s, c) writes its partial (running max m in log2 units, denominator
-//   l, un-normalised O) to slot s + c; a monotone staircase of pieces makes
-//   that index unique.
+//   Piece (s, c) writes its partial, one record per query row
+//   [un-normalised O (d floats) | running max m (log2 units) | denominator l |
+//   2 pad], to slot s + c; a monotone staircase of pieces makes that index
+//   unique.
 // After a grid-wide barrier every CTA merges a slice of all output rows over
 // the pieces of their segment: the log-sum-exp merge of the method ("LongSpec:
 // Long-Context Lossless Speculative Decoding with Efficient Drafting and
-// Verification", Korean summary section 2.C "aggregation").
+// Verification", Korean summary section 2.C "aggregation"). The records of a
+// slice are contiguous per piece, so one bulk copy per piece stages them in
+// shared memory before the reduction.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -26,6 +29,7 @@
 #include <stdint.h>
 
 #include "../../include/hta.h"
+#include "tc_ptx.cuh"
 
 namespace hta {
 
@@ -54,9 +58,7 @@ struct AttnParams {
     int32_t tile;          // keys per unit
     int32_t n_tree_tiles;  // ceil(T / tile) when include_tree
     // workspace
-    float *ws_o;  // [slots][rows_pg][d]
-    float *ws_m;  // [slots][rows_pg]
-    float *ws_l;  // [slots][rows_pg]
+    float *ws_rec;      // [slots][rows_pg][d + 4] partial records
     unsigned int *bar;  // [0] arrivals, [1] departures
     int64_t slots;
     int32_t *dev_err;
@@ -93,40 +95,42 @@ __device__ __forceinline__ int32_t clamp_len(const AttnParams &p, int32_t L) {
 
 // Builds, in shared memory, the clamped lengths lens_s[b] and the exclusive
 // prefix pre_s[b] = sum_{b' < b} Hkv * n_rg * seg_units(b'); pre_s[B] = U.
-// Must be called by every thread of the block. Reports bad lengths once (CTA 0).
-__device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int64_t *pre_s,
-                                      int64_t *scratch /* [blockDim.x] */) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    const int per = (p.B + nt - 1) / nt;
-    const int b0 = tid * per;
-    int64_t local = 0;
-    for (int b = b0; b < b0 + per && b < p.B; ++b) {
-        int32_t L = p.cache_lens[b];
-        if (L < 0 || (int64_t)L > p.Lmax) {
-            if (blockIdx.x == 0) flag_error(p.dev_err, HTA_DEVERR_CACHE_LEN);
-            L = L < 0 ? 0 : (int32_t)p.Lmax;
-        }
-        lens_s[b] = L;
-        local += (int64_t)p.Hkv * p.n_rg * seg_units(p, L);
-    }
-    scratch[tid] = local;
-    __syncthreads();
-    if (tid == 0) {
+// Warp 0 scans 32 sequences at a time with shuffles; every thread of the
+// block must call it (it ends with __syncthreads). Bad lengths are reported
+// once, by CTA 0.
+__device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int64_t *pre_s) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
         int64_t run = 0;
-        for (int i = 0; i < nt; ++i) {
-            int64_t v = scratch[i];
-            scratch[i] = run;
-            run += v;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            int64_t v = 0;
+            if (b < p.B) {
+                int32_t L = p.cache_lens[b];
+                if (L < 0 || (int64_t)L > p.Lmax) {
+                    if (blockIdx.x == 0) flag_error(p.dev_err, HTA_DEVERR_CACHE_LEN);
+                    L = L < 0 ? 0 : (int32_t)p.Lmax;
+                }
+                lens_s[b] = L;
+                v = (int64_t)p.Hkv * p.n_rg * seg_units(p, L);
+            }
+            int64_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (b < p.B) pre_s[b] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        pre_s[p.B] = run;
+        if (lane == 0) pre_s[p.B] = run;
     }
     __syncthreads();
-    int64_t run = scratch[tid];
-    for (int b = b0; b < b0 + per && b < p.B; ++b) {
-        pre_s[b] = run;
-        run += (int64_t)p.Hkv * p.n_rg * seg_units(p, lens_s[b]);
-    }
-    __syncthreads();
+}
+
+// shared-memory bytes of the schedule arrays for B sequences
+__host__ __device__ constexpr size_t sched_bytes(int B) {
+    return ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8;
 }
 
 __device__ __forceinline__ int64_t cta_lo(int64_t c, int64_t U, int64_t grid) {
@@ -233,109 +237,170 @@ __device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return se
 
 // ---------------------------------------------------------------- merge phase
 
-// Merges every output row handled by this CTA: rows are the packed rows of
-// all segments, linearised segment-major and split evenly over the grid.
-// One warp per row. Lane k first reads the running max and denominator of
-// piece k (32 pieces at a time) so the loads overlap; the weights are then
-// broadcast and each lane accumulates d/32 adjacent columns.
+// Merges every output row handled by this CTA. Rows are the packed rows of
+// all segments, linearised segment-major and split evenly over the grid. The
+// CTA walks its slice in chunks of consecutive rows of one segment: thread 0
+// bulk-copies the records of those rows from every piece of the segment into
+// `buf` (one copy per piece, all in flight together), then one warp per row
+// reduces them: M = max_k m_k, w_k = 2^(m_k - M), O = sum_k w_k O_k /
+// sum_k w_k l_k, LSE = (M + log2 sum_k w_k l_k) ln 2.
 template <int D>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
-                                   bool barrier_ok) {
-    constexpr int CPL = D / 32;  // columns per lane
+                                   bool barrier_ok, uint8_t *buf, uint32_t buf_bytes) {
+    constexpr int CPL = D / 32;        // columns per lane
+    constexpr int REC = D + 4;         // floats per record
+    constexpr uint32_t REC_BYTES = REC * 4;
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ int32_t ok_s;
     const int64_t n_seg = (int64_t)p.B * p.Hkv * p.n_rg;
-    const int64_t rows_total = n_seg * p.rows_pg;  // includes padding rows of short groups
+    const int64_t rows_total = n_seg * p.rows_pg;
     const int64_t grid = gridDim.x;
     const int64_t r0 = (blockIdx.x * rows_total) / grid;
     const int64_t r1 = ((blockIdx.x + 1) * rows_total) / grid;
     const int64_t U = pre_s[p.B];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    for (int64_t rr = r0 + warp; rr < r1; rr += nwarps) {
+    const uint32_t bar = tc::smem_u32(&mbar);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar, 1);
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0;
+
+    int64_t rr = r0;
+    while (rr < r1) {
         const int64_t seg = rr / p.rows_pg;
-        const int32_t lr = (int32_t)(rr - seg * p.rows_pg);
+        const int32_t lr_a = (int32_t)(rr - seg * p.rows_pg);
         const int32_t rg = (int32_t)(seg % p.n_rg);
         const int32_t kvh = (int32_t)((seg / p.n_rg) % p.Hkv);
         const int32_t b = (int32_t)(seg / ((int64_t)p.n_rg * p.Hkv));
-        if (lr >= rows_in_group(p, rg)) continue;
-        const int32_t r = rg * p.rows_pg + lr;  // packed row
-        const int32_t t = r / p.G, hq = kvh * p.G + (r - t * p.G);
-        const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
+        const int32_t nrows = rows_in_group(p, rg);
+        int64_t seg_stop = (seg + 1) * p.rows_pg;
+        if (seg_stop > r1) seg_stop = r1;
+        if (lr_a >= nrows) {  // padding rows of a short group
+            rr = seg_stop;
+            continue;
+        }
+        int32_t lr_end = (int32_t)(seg_stop - seg * p.rows_pg);
+        if (lr_end > nrows) lr_end = nrows;
 
         const int32_t su = seg_units(p, lens_s[b]);
         const int64_t sb = pre_s[b] + ((int64_t)kvh * p.n_rg + rg) * su;
-        int64_t c_first = 0, n_pieces = 0;
+        int64_t c_first = 0;
+        int32_t n_pieces = 0;
         if (su > 0 && barrier_ok) {
             c_first = cta_of_unit(sb, U, grid);
-            n_pieces = cta_of_unit(sb + su - 1, U, grid) - c_first + 1;
+            n_pieces = (int32_t)(cta_of_unit(sb + su - 1, U, grid) - c_first + 1);
         }
-        // pass 1: global max over pieces
-        float M = -INFINITY;
-        for (int64_t k0 = 0; k0 < n_pieces; k0 += 32) {
-            const int64_t c = c_first + k0 + lane;
-            float m = -INFINITY;
-            if (k0 + lane < n_pieces && cta_lo(c, U, grid) != cta_lo(c + 1, U, grid))
-                m = p.ws_m[slot_of(seg, c) * p.rows_pg + lr];
-            M = fmaxf(M, m);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        // pass 2: weights, denominator, weighted sum of the un-normalised outputs
-        float den = 0.f;
-        float acc[CPL];
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
-        if (M > -INFINITY) {
-            for (int64_t k0 = 0; k0 < n_pieces; k0 += 32) {
-                const int64_t c = c_first + k0 + lane;
-                float w = 0.f;
-                if (k0 + lane < n_pieces && cta_lo(c, U, grid) != cta_lo(c + 1, U, grid)) {
-                    const int64_t sidx = slot_of(seg, c) * p.rows_pg + lr;
-                    const float m = p.ws_m[sidx];
-                    if (m > -INFINITY) {
-                        w = exp2f(m - M);
-                        den += w * p.ws_l[sidx];
-                    }
+        const uint32_t per_row = (uint32_t)(n_pieces > 0 ? n_pieces : 1) * REC_BYTES;
+        int32_t nr = (int32_t)(buf_bytes / per_row);
+        if (nr > lr_end - lr_a) nr = lr_end - lr_a;
+        if (nr < 1) nr = 1;  // a single row always fits: pieces <= grid
+
+        // stage the records of rows [lr_a, lr_a + nr) of every piece
+        if (threadIdx.x == 0) {
+            int ok = 1;
+            if (n_pieces > 0) {
+                uint32_t bytes = 0;
+                for (int k = 0; k < n_pieces; ++k)
+                    if (cta_lo(c_first + k, U, grid) != cta_lo(c_first + k + 1, U, grid)) bytes += nr * REC_BYTES;
+                tc::fence_proxy_async_all();
+                tc::mbar_arrive_expect_tx(bar, bytes);
+                for (int k = 0; k < n_pieces; ++k) {
+                    const int64_t c = c_first + k;
+                    if (cta_lo(c, U, grid) == cta_lo(c + 1, U, grid)) continue;
+                    const float *src = p.ws_rec + (slot_of(seg, c) * p.rows_pg + lr_a) * REC;
+                    tc::bulk_load(tc::smem_u32(buf + (uint32_t)k * nr * REC_BYTES), src, nr * REC_BYTES, bar);
                 }
-                const int nk = (int)((n_pieces - k0) < 32 ? (n_pieces - k0) : 32);
-                for (int k = 0; k < nk; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, w, k);
-                    if (wk == 0.f) continue;
-                    const int64_t sidx = slot_of(seg, c_first + k0 + k) * p.rows_pg + lr;
-                    const float *o = p.ws_o + sidx * D + lane * CPL;
-                    if constexpr (CPL == 4) {
-                        const float4 v = *reinterpret_cast<const float4 *>(o);
-                        acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
-                    } else {
-                        const float2 v = *reinterpret_cast<const float2 *>(o);
-                        acc[0] += wk * v.x; acc[1] += wk * v.y;
+                const uint64_t t0 = globaltimer_ns();
+                while (!tc::mbar_try_wait(bar, phase)) {
+                    if (globaltimer_ns() - t0 > 1000000000ull) {
+                        ok = 0;
+                        flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
+                        break;
                     }
                 }
             }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            ok_s = ok;
         }
-        float lse, inv;
-        if (!barrier_ok) {
-            lse = __int_as_float(0x7fc00000);
-            inv = __int_as_float(0x7fc00000);
-        } else if (den > 0.f) {
-            lse = (M + log2f(den)) * kLn2;
-            inv = 1.f / den;
-        } else {
-            lse = -INFINITY;  // no visible key: empty softmax
-            inv = 0.f;
-        }
-        if (p.out_fp32) {
-            float *o = (float *)p.out_o + out_row * D + lane * CPL;
+        __syncthreads();
+        if (n_pieces > 0) phase ^= 1;
+        const bool staged = ok_s != 0;
+
+        for (int i = warp; i < nr; i += nwarps) {
+            const int32_t lr = lr_a + i;
+            const int32_t r = rg * p.rows_pg + lr;  // packed row
+            const int32_t t = r / p.G, hq = kvh * p.G + (r - t * p.G);
+            const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
+            // global max over pieces
+            float M = -INFINITY;
+            for (int k0 = 0; k0 < n_pieces; k0 += 32) {
+                const int k = k0 + lane;
+                float m = -INFINITY;
+                if (k < n_pieces && cta_lo(c_first + k, U, grid) != cta_lo(c_first + k + 1, U, grid))
+                    m = reinterpret_cast<const float *>(buf + ((uint32_t)k * nr + i) * REC_BYTES)[D];
+                M = fmaxf(M, m);
+            }
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) o[k] = acc[k] * inv;
-        } else {
-            __nv_bfloat16 *o = (__nv_bfloat16 *)p.out_o + out_row * D + lane * CPL;
+            for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            float den = 0.f, acc[CPL];
 #pragma unroll
-            for (int k = 0; k < CPL; k += 2)
-                *reinterpret_cast<__nv_bfloat162 *>(o + k) =
-                    __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+            for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
+            if (M > -INFINITY) {
+                for (int k0 = 0; k0 < n_pieces; k0 += 32) {
+                    const int k = k0 + lane;
+                    float w = 0.f;
+                    if (k < n_pieces && cta_lo(c_first + k, U, grid) != cta_lo(c_first + k + 1, U, grid)) {
+                        const float *rec = reinterpret_cast<const float *>(buf + ((uint32_t)k * nr + i) * REC_BYTES);
+                        if (rec[D] > -INFINITY) {
+                            w = exp2f(rec[D] - M);
+                            den += w * rec[D + 1];
+                        }
+                    }
+                    const int nk = n_pieces - k0 < 32 ? n_pieces - k0 : 32;
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const float wk = __shfl_sync(0xffffffffu, w, kk);
+                        if (wk == 0.f) continue;
+                        const float *o = reinterpret_cast<const float *>(
+                                             buf + ((uint32_t)(k0 + kk) * nr + i) * REC_BYTES) + lane * CPL;
+                        if constexpr (CPL == 4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(o);
+                            acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
+                        } else {
+                            const float2 v = *reinterpret_cast<const float2 *>(o);
+                            acc[0] += wk * v.x; acc[1] += wk * v.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            }
+            float lse, inv;
+            if (!barrier_ok || !staged) {
+                lse = __int_as_float(0x7fc00000);
+                inv = __int_as_float(0x7fc00000);
+            } else if (den > 0.f) {
+                lse = (M + log2f(den)) * kLn2;
+                inv = 1.f / den;
+            } else {
+                lse = -INFINITY;  // no visible key: empty softmax
+                inv = 0.f;
+            }
+            if (p.out_fp32) {
+                float *o = (float *)p.out_o + out_row * D + lane * CPL;
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) o[k] = acc[k] * inv;
+            } else {
+                __nv_bfloat16 *o = (__nv_bfloat16 *)p.out_o + out_row * D + lane * CPL;
+#pragma unroll
+                for (int k = 0; k < CPL; k += 2)
+                    *reinterpret_cast<__nv_bfloat162 *>(o + k) =
+                        __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+            }
+            if (lane == 0) p.out_lse[out_row] = lse;
         }
-        if (lane == 0) p.out_lse[out_row] = lse;
+        __syncthreads();  // the buffer is reused by the next chunk
+        rr = seg * p.rows_pg + lr_a + nr;
     }
 }
 

@@ -219,13 +219,12 @@ __device__ __forceinline__ void cc_emit(const AttnParams &p, const RowState<D> &
         const int lr = warp * kRowsPerWarp + i;
         if (lr >= nrows) continue;
         if (!direct) {
-            const int64_t sidx = slot * p.rows_pg + lr;
-            float *o = p.ws_o + sidx * D + lane * CPL;
+            float *rec = p.ws_rec + (slot * p.rows_pg + lr) * (D + 4);
 #pragma unroll
-            for (int k = 0; k < CPL; ++k) o[k] = st.acc[i][k];
+            for (int k = 0; k < CPL; ++k) rec[lane * CPL + k] = st.acc[i][k];
             if (lane == 0) {
-                p.ws_m[sidx] = st.m[i];
-                p.ws_l[sidx] = st.l[i];
+                rec[D] = st.m[i];
+                rec[D + 1] = st.l[i];
             }
         } else {
             const int r = rg * p.rows_pg + lr, t = r / p.G, hq = kvh * p.G + (r - t * p.G);
@@ -252,7 +251,7 @@ __device__ __forceinline__ void cc_emit(const AttnParams &p, const RowState<D> &
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ AttnParams p, int direct) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     CcSmem<D> &sm = *reinterpret_cast<CcSmem<D> *>(smem_raw);
     RowState<D> st;
 
@@ -280,8 +279,7 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
     int32_t *lens_s = reinterpret_cast<int32_t *>(smem_raw + sizeof(CcSmem<D>));
     int64_t *pre_s = reinterpret_cast<int64_t *>(smem_raw + sizeof(CcSmem<D>) +
                                                  ((p.B * 4 + 15) / 16) * 16);
-    int64_t *scratch = pre_s + p.B + 1;
-    build_schedule(p, lens_s, pre_s, scratch);
+    build_schedule(p, lens_s, pre_s);
     const int64_t U = pre_s[p.B];
     const int64_t grid = gridDim.x;
     int64_t u = cta_lo(blockIdx.x, U, grid);
@@ -296,13 +294,14 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
         u = piece_end;
     }
     const bool ok = grid_barrier(p);
-    merge_phase<D>(p, lens_s, pre_s, ok);
+    __syncthreads();  // the tile buffers become the merge staging area
+    merge_phase<D>(p, lens_s, pre_s, ok, smem_raw, (uint32_t)sizeof(CcSmem<D>));
     grid_barrier_depart(p);
 }
 
 template <int D>
 size_t cc_smem_bytes(int B) {
-    return sizeof(CcSmem<D>) + ((B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8 + kThreads * 8;
+    return sizeof(CcSmem<D>) + sched_bytes(B);
 }
 
 template <int D>

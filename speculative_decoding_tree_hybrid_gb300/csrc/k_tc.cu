@@ -318,8 +318,11 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
         uint32_t w4[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) w4[k] = (tree && valid) ? (t.unit == 0 ? mw[k] : mw[4 + k]) : 0xffffffffu;
-        // scaled scores (base 2), masked keys -inf
-        float m_tile = -INFINITY;
+        // scaled scores (base 2), masked keys -inf; eight partial maxima
+        // keep the max reduction off one long dependency chain
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -328,9 +331,11 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
                 const bool vis = col < nvalid && ((w4[k] >> e) & 1u);
                 const float x = vis ? __uint_as_float(s[k][e]) * c2 : -INFINITY;
                 s[k][e] = __float_as_uint(x);
-                m_tile = fmaxf(m_tile, x);
+                mx[e & 7] = fmaxf(mx[e & 7], x);
             }
         }
+        const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_run, m_tile);
         const bool need = m_new > m_run + kRescaleThreshold;
         float alpha = 1.f;
@@ -369,7 +374,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             fence_proxy_async_smem();
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float lsum = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
             uint32_t pk[32];
@@ -377,12 +382,12 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             for (int e = 0; e < 32; ++e) {
                 const float p0 = ex2(__uint_as_float(s[2 * k2 + (e >> 4)][(e & 15) * 2]) - m_use);
                 const float p1 = ex2(__uint_as_float(s[2 * k2 + (e >> 4)][(e & 15) * 2 + 1]) - m_use);
-                lsum += p0 + p1;
+                ls[e & 3] += p0 + p1;
                 pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st32(tS + 32 * k2, pk);
         }
-        l_run += lsum;
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_addr(sh.p_full[h]));
@@ -392,8 +397,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             ok = wait_bar(bar_addr(sh.o_done[h]), t.q & 1, abort, p.dev_err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int64_t sidx = slot_of(t.seg, blockIdx.x) * p.rows_pg + r_local;
-            float *dst = p.ws_o + sidx * 128;
+            float *rec = p.ws_rec + (slot_of(t.seg, blockIdx.x) * p.rows_pg + r_local) * 132;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 uint32_t o[32];
@@ -403,13 +407,10 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<uint4 *>(dst + 32 * k + e) = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                        *reinterpret_cast<uint4 *>(rec + 32 * k + e) = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
                 }
             }
-            if (valid) {
-                p.ws_m[sidx] = m_run;
-                p.ws_l[sidx] = l_run;
-            }
+            if (valid) *reinterpret_cast<float2 *>(rec + 128) = make_float2(m_run, l_run);
             tc_fence_before();
             mbar_arrive(bar_addr(sh.o_free[h]));
         }
@@ -424,7 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     TcShared &sh = *reinterpret_cast<TcShared *>(smem + kOffShared);
     int32_t *lens_s = reinterpret_cast<int32_t *>(smem + kOffSched);
     int64_t *pre_s = reinterpret_cast<int64_t *>(smem + kOffSched + ((p.B * 4 + 15) / 16) * 16);
-    int64_t *scratch = pre_s + p.B + 1;
     const uint32_t sQ = smem_u32(smem + kOffQ), ring = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5;
 
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before();
     }
-    build_schedule(p, lens_s, pre_s, scratch);  // ends with __syncthreads
+    build_schedule(p, lens_s, pre_s);  // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const int64_t U = pre_s[p.B];
@@ -496,12 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
     const bool ok = grid_barrier(p);
-    merge_phase<128>(p, lens_s, pre_s, ok);
+    // Q and the K/V ring are idle now: they stage the merge
+    merge_phase<128>(p, lens_s, pre_s, ok, smem + kOffQ, kOffShared - kOffQ);
     grid_barrier_depart(p);
 }
 
 size_t tc_smem_bytes(int B) {
-    return 1024 + kOffSched + ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8 + kThreads * 8;
+    return 1024 + kOffSched + sched_bytes(B);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
