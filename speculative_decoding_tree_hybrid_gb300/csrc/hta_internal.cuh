@@ -93,12 +93,13 @@ __device__ __forceinline__ int32_t clamp_len(const AttnParams &p, int32_t L) {
     return L;
 }
 
-// Builds, in shared memory, the clamped lengths lens_s[b] and the exclusive
-// prefix pre_s[b] = sum_{b' < b} Hkv * n_rg * seg_units(b'); pre_s[B] = U.
+// Builds, in shared memory, the clamped lengths lens_s[b], the exclusive
+// prefix pre_s[b] = sum_{b' < b} Hkv * n_rg * seg_units(b') with pre_s[B] = U,
+// and the CTA boundaries lo_s[c] = floor(c * U / grid) for c = 0..grid.
 // Warp 0 scans 32 sequences at a time with shuffles; every thread of the
 // block must call it (it ends with __syncthreads). Bad lengths are reported
 // once, by CTA 0.
-__device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int64_t *pre_s) {
+__device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int64_t *pre_s, int64_t *lo_s) {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int64_t run = 0;
@@ -126,24 +127,25 @@ __device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int6
         if (lane == 0) pre_s[p.B] = run;
     }
     __syncthreads();
+    const int64_t U = pre_s[p.B];
+    for (int c = threadIdx.x; c <= (int)gridDim.x; c += blockDim.x) lo_s[c] = ((int64_t)c * U) / gridDim.x;
+    __syncthreads();
 }
 
-// shared-memory bytes of the schedule arrays for B sequences
-__host__ __device__ constexpr size_t sched_bytes(int B) {
-    return ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8;
+// shared-memory bytes of the schedule arrays for B sequences and `grid` CTAs
+__host__ __device__ constexpr size_t sched_bytes(int B, int grid) {
+    return ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8 + (size_t)(grid + 1) * 8;
 }
 
-__device__ __forceinline__ int64_t cta_lo(int64_t c, int64_t U, int64_t grid) {
-    return (c * U) / grid;
-}
-
-// CTA that owns unit u (the unique c with lo(c) <= u < lo(c+1)).
-__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t grid) {
-    int64_t c = (u * grid) / U;
-    if (c >= grid) c = grid - 1;
-    while (c + 1 < grid && cta_lo(c + 1, U, grid) <= u) ++c;
-    while (c > 0 && cta_lo(c, U, grid) > u) --c;
-    return c;
+// CTA that owns unit u: the largest c < grid with lo_s[c] <= u (CTAs with an
+// empty range share their lo with the next CTA and are never returned).
+__device__ __forceinline__ int32_t cta_of_unit(int64_t u, const int64_t *lo_s, int32_t grid) {
+    int32_t lo = 0, hi = grid - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (lo_s[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 // Sequence containing unit u: largest b with pre_s[b] <= u (binary search).
@@ -246,7 +248,7 @@ __device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return se
 // sum_k w_k l_k, LSE = (M + log2 sum_k w_k l_k) ln 2.
 template <int D>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
-                                   bool barrier_ok, uint8_t *buf, uint32_t buf_bytes) {
+                                   const int64_t *lo_s, bool barrier_ok, uint8_t *buf, uint32_t buf_bytes) {
     constexpr int CPL = D / 32;        // columns per lane
     constexpr int REC = D + 4;         // floats per record
     constexpr uint32_t REC_BYTES = REC * 4;
@@ -254,12 +256,13 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
     __shared__ int32_t ok_s;
     const int64_t n_seg = (int64_t)p.B * p.Hkv * p.n_rg;
     const int64_t rows_total = n_seg * p.rows_pg;
-    const int64_t grid = gridDim.x;
+    const int32_t grid = gridDim.x;
     const int64_t r0 = (blockIdx.x * rows_total) / grid;
     const int64_t r1 = ((blockIdx.x + 1) * rows_total) / grid;
-    const int64_t U = pre_s[p.B];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const uint32_t bar = tc::smem_u32(&mbar);
+    // a piece exists for every CTA whose unit range is not empty
+    auto has_units = [&](int64_t c) { return lo_s[c] != lo_s[c + 1]; };
     if (threadIdx.x == 0) {
         tc::mbar_init(bar, 1);
         tc::mbar_fence_init();
@@ -289,8 +292,8 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
         int64_t c_first = 0;
         int32_t n_pieces = 0;
         if (su > 0 && barrier_ok) {
-            c_first = cta_of_unit(sb, U, grid);
-            n_pieces = (int32_t)(cta_of_unit(sb + su - 1, U, grid) - c_first + 1);
+            c_first = cta_of_unit(sb, lo_s, grid);
+            n_pieces = cta_of_unit(sb + su - 1, lo_s, grid) - (int32_t)c_first + 1;
         }
         const uint32_t per_row = (uint32_t)(n_pieces > 0 ? n_pieces : 1) * REC_BYTES;
         int32_t nr = (int32_t)(buf_bytes / per_row);
@@ -303,12 +306,12 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
             if (n_pieces > 0) {
                 uint32_t bytes = 0;
                 for (int k = 0; k < n_pieces; ++k)
-                    if (cta_lo(c_first + k, U, grid) != cta_lo(c_first + k + 1, U, grid)) bytes += nr * REC_BYTES;
+                    if (has_units(c_first + k)) bytes += nr * REC_BYTES;
                 tc::fence_proxy_async_all();
                 tc::mbar_arrive_expect_tx(bar, bytes);
                 for (int k = 0; k < n_pieces; ++k) {
                     const int64_t c = c_first + k;
-                    if (cta_lo(c, U, grid) == cta_lo(c + 1, U, grid)) continue;
+                    if (!has_units(c)) continue;
                     const float *src = p.ws_rec + (slot_of(seg, c) * p.rows_pg + lr_a) * REC;
                     tc::bulk_load(tc::smem_u32(buf + (uint32_t)k * nr * REC_BYTES), src, nr * REC_BYTES, bar);
                 }
@@ -337,7 +340,7 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
             for (int k0 = 0; k0 < n_pieces; k0 += 32) {
                 const int k = k0 + lane;
                 float m = -INFINITY;
-                if (k < n_pieces && cta_lo(c_first + k, U, grid) != cta_lo(c_first + k + 1, U, grid))
+                if (k < n_pieces && has_units(c_first + k))
                     m = reinterpret_cast<const float *>(buf + ((uint32_t)k * nr + i) * REC_BYTES)[D];
                 M = fmaxf(M, m);
             }
@@ -350,7 +353,7 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                 for (int k0 = 0; k0 < n_pieces; k0 += 32) {
                     const int k = k0 + lane;
                     float w = 0.f;
-                    if (k < n_pieces && cta_lo(c_first + k, U, grid) != cta_lo(c_first + k + 1, U, grid)) {
+                    if (k < n_pieces && has_units(c_first + k)) {
                         const float *rec = reinterpret_cast<const float *>(buf + ((uint32_t)k * nr + i) * REC_BYTES);
                         if (rec[D] > -INFINITY) {
                             w = exp2f(rec[D] - M);

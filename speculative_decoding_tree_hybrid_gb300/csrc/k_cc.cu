@@ -279,11 +279,10 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
     int32_t *lens_s = reinterpret_cast<int32_t *>(smem_raw + sizeof(CcSmem<D>));
     int64_t *pre_s = reinterpret_cast<int64_t *>(smem_raw + sizeof(CcSmem<D>) +
                                                  ((p.B * 4 + 15) / 16) * 16);
-    build_schedule(p, lens_s, pre_s);
-    const int64_t U = pre_s[p.B];
-    const int64_t grid = gridDim.x;
-    int64_t u = cta_lo(blockIdx.x, U, grid);
-    const int64_t u_end = cta_lo(blockIdx.x + 1, U, grid);
+    int64_t *lo_s = pre_s + p.B + 1;
+    build_schedule(p, lens_s, pre_s, lo_s);
+    int64_t u = lo_s[blockIdx.x];
+    const int64_t u_end = lo_s[blockIdx.x + 1];
     while (u < u_end) {
         const UnitPos pos = locate_unit(p, u, lens_s, pre_s);
         const int64_t seg_end = pos.seg_begin + pos.seg_units;
@@ -295,18 +294,18 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
     }
     const bool ok = grid_barrier(p);
     __syncthreads();  // the tile buffers become the merge staging area
-    merge_phase<D>(p, lens_s, pre_s, ok, smem_raw, (uint32_t)sizeof(CcSmem<D>));
+    merge_phase<D>(p, lens_s, pre_s, lo_s, ok, smem_raw, (uint32_t)sizeof(CcSmem<D>));
     grid_barrier_depart(p);
 }
 
 template <int D>
-size_t cc_smem_bytes(int B) {
-    return sizeof(CcSmem<D>) + sched_bytes(B);
+size_t cc_smem_bytes(int B, int grid) {
+    return sizeof(CcSmem<D>) + sched_bytes(B, grid);
 }
 
 template <int D>
 cudaError_t cc_launch_t(const AttnParams &p, bool direct, int grid, cudaStream_t stream) {
-    const size_t smem = cc_smem_bytes<D>(p.B);
+    const size_t smem = cc_smem_bytes<D>(p.B, grid);
     cudaError_t e = cudaFuncSetAttribute(k_cc_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -325,14 +324,15 @@ cudaError_t cc_launch_t(const AttnParams &p, bool direct, int grid, cudaStream_t
 
 template <int D>
 int cc_max_grid_t(int B, int num_sms) {
-    const size_t smem = cc_smem_bytes<D>(B);
+    // the boundary table grows with the grid: size it for 8 CTAs per SM
+    const size_t smem = cc_smem_bytes<D>(B, 8 * num_sms);
     if (cudaFuncSetAttribute(k_cc_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_cc_attn<D>, kThreads, smem) != cudaSuccess)
         return 0;
-    return occ * num_sms;
+    return (occ < 8 ? occ : 8) * num_sms;
 }
 
 }  // namespace

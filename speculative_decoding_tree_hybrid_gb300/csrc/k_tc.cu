@@ -4,7 +4,7 @@
 // Efficient Drafting and Verification", Korean summary section 2.C, Dutch
 // summary Methodologie section 3) splits the verification attention into an
 // unmasked pass over the long cached prefix and a masked pass over the tree
-// tokens, merged by log-sum-exp. Here both passes are 128-key tiles of one
+// tokens, merged by log-sum-exp. Here both passes are 64-key tiles of one
 // persistent cooperative grid (one CTA per SM, a static split-KV schedule
 // balanced by tile count, see hta_internal.cuh), and the cross-split and
 // cross-part merge runs after a grid barrier in the same launch.
@@ -12,21 +12,23 @@
 // One CTA works on a row group of up to 256 packed query rows of one KV head
 // (row r = t*G + g, so every K/V tile is shared by all G query heads of the
 // tree), as two 128-row halves:
-//   warp 0        TMA producer: K and V tiles (128 keys x 128 dims, bf16,
-//                 128-byte swizzle) into a 4-stage shared-memory ring;
-//   warp 1        MMA issuer (one thread): S_h = Q_h K^T into tensor memory,
-//                 then O_h += P_h V with P_h read from tensor memory;
+//   warp 0        TMA producer: K and V tiles (64 keys x 128 dims, bf16,
+//                 128-byte swizzle) into a 9-stage shared-memory ring;
+//   warp 1        MMA issuer (one thread): S(h,i) = Q_h K(i)^T into tensor
+//                 memory, then O_h += P(h,i) V(i) with P read from tensor memory;
 //   warps 4-7     softmax of half 0, one query row per thread;
 //   warps 8-11    softmax of half 1.
-// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each; P_h
-// (bf16) overwrites the first 64 columns of S_h. The MMA order
-// PV(0,i), S(0,i+1), PV(1,i), S(1,i+1) lets the softmax of one half overlap
-// the other half's MMAs, and tensor-core operations of one thread execute in
-// issue order, so S(h,i+1) never overtakes PV(h,i) that still reads P_h.
+// Tensor memory (512 columns): S(0,even) | S(0,odd) | S(1,even) | S(1,odd),
+// 64 columns each, then O_0 | O_1, 128 columns each. P(h,i) (bf16) overwrites
+// the first 32 columns of its S buffer. With two S buffers per half the
+// tensor core computes S(h,i+1) while the softmax works on S(h,i); the MMA
+// thread issues PV(h,i) and then S(h,i+2) into the buffer PV(h,i) reads,
+// which is safe because tensor-core operations of one thread run in issue
+// order.
 // The softmax keeps the row max in base 2 (scores times scale*log2 e) and
 // rescales O in tensor memory only when the max grows by more than 8
-// (factor 256), which leaves the result exact because numerator and
-// denominator share the stale max.
+// (factor 256); numerator and denominator share the stale max, so the result
+// is exact.
 //
 // Every wait is bounded (~1 s of device time); on expiry the kernel sets
 // HTA_DEVERR_TIMEOUT, waits for its own copies in flight, frees its tensor
@@ -44,20 +46,22 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTile = 128;          // keys per tile
+constexpr int kTile = 64;           // keys per tile
 constexpr int kHalf = 128;          // query rows per MMA
 constexpr int kMaxRows = 256;       // rows per row group
-constexpr int kStages = 4;          // K/V ring stages
+constexpr int kStages = 9;          // K/V ring stages
 constexpr int kThreads = 384;
-constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one K or V tile
-constexpr uint32_t kSubBytes = 128 * 64 * 2;    // one 64-dim swizzled sub-tile
+constexpr uint32_t kTileBytes = 64 * 128 * 2;    // one K or V tile
+constexpr uint32_t kSubBytes = 64 * 64 * 2;      // one 64-dim swizzled sub-tile of it
+constexpr uint32_t kQHalfBytes = 128 * 128 * 2;  // Q rows of one half
+constexpr uint32_t kQSubBytes = 128 * 64 * 2;    // one 64-dim sub-tile of them
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffRing = 2 * kQHalfBytes;
 constexpr uint32_t kOffShared = kOffRing + kStages * kTileBytes;
 constexpr uint32_t kSharedBytes = 512;
 constexpr uint32_t kOffSched = kOffShared + kSharedBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;
+constexpr uint32_t kColO = 256;     // S buffers take columns 0..255
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -68,7 +72,8 @@ struct TcMaps {
 struct TcShared {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t s_full[2], p_full[2], o_done[2], o_free[2], q_full[2];
+    uint64_t s_full[2][2], p_full[2][2];  // [half][S buffer]
+    uint64_t pv_done[2], o_done[2], o_free[2], q_full[2];
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -191,59 +196,70 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     }
 }
 
+// Issue order per half: S(0), S(1), PV(0), S(2), PV(1), S(3), ... where the
+// first tile of a piece waits for the previous tile's PV instead (its Q is
+// loaded only after the previous piece's output was read). The two halves
+// alternate op by op.
 __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
                            int halves, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
     Cursor c;
     cursor_init(c, u0, u1);
-    TileInfo cur, nxt;
-    bool has_cur = cursor_next(c, p, lens_s, pre_s, cur);
-    if (!has_cur) return;
+    TileInfo cur, n1, n2;
+    if (!cursor_next(c, p, lens_s, pre_s, cur)) return;
+    bool has1 = cursor_next(c, p, lens_s, pre_s, n1);
+    bool has2 = has1 && cursor_next(c, p, lens_s, pre_s, n2);
 
-    // S_h(i) = Q_h K(i)^T
-    auto issue_s = [&](int h, uint32_t i, const TileInfo &ti) -> bool {
-        const uint32_t n = 2 * i, st = n % kStages, round = n / kStages;
+    // S(h,j) = Q_h K(j)^T into S buffer j&1 of half h
+    auto issue_s = [&](int h, uint32_t j, const TileInfo &tj) -> bool {
+        const uint32_t n = 2 * j, st = n % kStages, round = n / kStages;
         if (h == 0 && !wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return false;
-        if (ti.first && !wait_bar(bar_addr(sh.q_full[h]), ti.q & 1, abort, p.dev_err)) return false;
+        if (tj.first && !wait_bar(bar_addr(sh.q_full[h]), tj.q & 1, abort, p.dev_err)) return false;
         tc_fence_after();
-        const uint32_t qa = sQ + h * kTileBytes, kb = ring + st * kTileBytes;
+        const uint32_t qa = sQ + h * kQHalfBytes, kb = ring + st * kTileBytes;
+        const uint32_t d = tmem + h * 128 + (j & 1) * 64;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColS + h * 128, smem_desc_sw128(qa + off, 16, 1024),
-                   smem_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0);
-        }
-        mma_commit(bar_addr(sh.s_full[h]));
+        for (int kk = 0; kk < 8; ++kk)
+            mma_ss(d, smem_desc_sw128(qa + (kk >> 2) * kQSubBytes + (kk & 3) * 32, 16, 1024),
+                   smem_desc_sw128(kb + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
+        mma_commit(bar_addr(sh.s_full[h][j & 1]));
         if (h == halves - 1) mma_commit(bar_addr(sh.empty[st]));
         return true;
     };
 
     for (int h = 0; h < halves; ++h)
         if (!issue_s(h, 0, cur)) return;
+    if (has1 && !n1.first)
+        for (int h = 0; h < halves; ++h)
+            if (!issue_s(h, 1, n1)) return;
     for (uint32_t i = 0;; ++i) {
-        const bool has_next = cursor_next(c, p, lens_s, pre_s, nxt);
-        const uint32_t n = 2 * i + 1, st = n % kStages, round = n / kStages;
-        if (!wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return;
-        const uint32_t vb = ring + st * kTileBytes;
+        const uint32_t nv = 2 * i + 1, stv = nv % kStages, rv = nv / kStages;
+        if (!wait_bar(bar_addr(sh.full[stv]), rv & 1, abort, p.dev_err)) return;
+        const uint32_t vb = ring + stv * kTileBytes;
         for (int h = 0; h < halves; ++h) {
-            if (!wait_bar(bar_addr(sh.p_full[h]), i & 1, abort, p.dev_err)) return;
+            if (!wait_bar(bar_addr(sh.p_full[h][i & 1]), (i >> 1) & 1, abort, p.dev_err)) return;
             if (cur.first && cur.q > 0 &&
                 !wait_bar(bar_addr(sh.o_free[h]), (cur.q - 1) & 1, abort, p.dev_err))
                 return;
             tc_fence_after();
+            const uint32_t pa = tmem + h * 128 + (i & 1) * 64;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ts(tmem + kColO + h * 128, tmem + kColS + h * 128 + kk * 8,
-                       smem_desc_sw128(vb + kk * 2048, kSubBytes, 1024), idesc_pv,
-                       (!cur.first || kk > 0) ? 1u : 0u);
-            if (h == halves - 1) mma_commit(bar_addr(sh.empty[st]));
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tmem + kColO + h * 128, pa + kk * 8, smem_desc_sw128(vb + kk * 2048, kSubBytes, 1024),
+                       idesc_pv, (!cur.first || kk > 0) ? 1u : 0u);
+            mma_commit(bar_addr(sh.pv_done[h]));
+            if (h == halves - 1) mma_commit(bar_addr(sh.empty[stv]));
             if (cur.last) mma_commit(bar_addr(sh.o_done[h]));
-            if (has_next && !issue_s(h, i + 1, nxt)) return;
+            if (has1 && n1.first && !issue_s(h, i + 1, n1)) return;
+            if (has2 && !n2.first && !issue_s(h, i + 2, n2)) return;
         }
-        if (!has_next) break;
-        cur = nxt;
+        if (!has1) break;
+        cur = n1;
+        has1 = has2;
+        n1 = n2;
+        has2 = has2 && cursor_next(c, p, lens_s, pre_s, n2);
     }
 }
 
@@ -254,7 +270,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     const int row = wq * 32 + lane;  // row of this half == TMEM lane
     const int tid_wg = threadIdx.x & 127;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + kColS + h * 128;
+    const uint32_t tS = tmem + lane_off + h * 128;  // + 64 for the odd S buffer
     const uint32_t tO = tmem + lane_off + kColO + h * 128;
     const int n_tree = p.include_tree ? p.n_tree_tiles : 0;
     const float c2 = p.scale_log2;
@@ -267,6 +283,8 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     bool o_valid = false, valid = false;
     int r_local = 0;
     uint32_t mw[HTA_TMAX / 32];
+#pragma unroll
+    for (int w = 0; w < HTA_TMAX / 32; ++w) mw[w] = 0u;
 
     while (cursor_next(c, p, lens_s, pre_s, t)) {
         if (t.first) {
@@ -276,16 +294,19 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             const int r = t.rg * p.rows_pg + r_local;
             const int tn = valid ? r / p.G : 0;
             const int hq = t.kvh * p.G + (r - tn * p.G);
-            // this row of Q_h, 128-byte swizzled, zero for padding rows
+            // this row of Q_h, 128-byte swizzled, zero for padding rows; all
+            // sixteen loads are in flight before the first store
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 p.q + (((int64_t)t.b * p.T + tn) * p.Hq + hq) * 128);
+            uint4 qv[16];
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) qv[ch] = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) {
-                const uint4 v = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
-                const uint32_t dst = sQ + h * kTileBytes + (ch >> 3) * kSubBytes + row * 128 +
+                const uint32_t dst = sQ + h * kQHalfBytes + (ch >> 3) * kQSubBytes + row * 128 +
                                      (((ch & 7) ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                             "r"(v.z), "r"(v.w)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[ch].x),
+                             "r"(qv[ch].y), "r"(qv[ch].z), "r"(qv[ch].w)
                              : "memory");
             }
             fence_proxy_async_smem();
@@ -302,40 +323,47 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
         const bool tree = t.unit < n_tree;
         const int j0 = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int nvalid = tree ? min(kTile, p.T - j0) : min(kTile, t.Lb - j0);
+        const uint32_t buf = gi & 1;
 
-        bool ok = wait_bar(bar_addr(sh.s_full[h]), gi & 1, abort, p.dev_err);
+        bool ok = wait_bar(bar_addr(sh.s_full[h][buf]), (gi >> 1) & 1, abort, p.dev_err);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld32(tS + 32 * k, s[k]);
+        uint32_t s[2][32];
+        tmem_ld32(tS + buf * 64, s[0]);
+        tmem_ld32(tS + buf * 64 + 32, s[1]);
         tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) reg_fence32(s[k]);
+        reg_fence32(s[0]);
+        reg_fence32(s[1]);
 
-        // mask words of this tile (a tree has at most two tiles of 128 keys);
-        // rows past the group see every key (their result is discarded)
-        uint32_t w4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w4[k] = (tree && valid) ? (t.unit == 0 ? mw[k] : mw[4 + k]) : 0xffffffffu;
-        // scaled scores (base 2), masked keys -inf; eight partial maxima
-        // keep the max reduction off one long dependency chain
+        // raw-score max (the scale is positive); masked keys become -inf
         float mx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+        if (!tree && nvalid == kTile) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 2; ++k)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int col = 32 * k + e;
-                const bool vis = col < nvalid && ((w4[k] >> e) & 1u);
-                const float x = vis ? __uint_as_float(s[k][e]) * c2 : -INFINITY;
-                s[k][e] = __float_as_uint(x);
-                mx[e & 7] = fmaxf(mx[e & 7], x);
+                for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(s[k][e]));
+        } else {
+            // mask words of this tile: a tree has at most four tiles of 64 keys;
+            // rows past the group see every key (their result is discarded)
+            uint32_t w2[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t w = t.unit == 0 ? mw[k] : t.unit == 1 ? mw[2 + k] : t.unit == 2 ? mw[4 + k] : mw[6 + k];
+                w2[k] = (tree && valid) ? w : 0xffffffffu;
             }
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const bool vis = (32 * k + e) < nvalid && ((w2[k] >> e) & 1u);
+                    if (!vis) s[k][e] = 0xff800000u;  // -inf
+                    mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(s[k][e]));
+                }
         }
         const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c2;
         const float m_new = fmaxf(m_run, m_tile);
         const bool need = m_new > m_run + kRescaleThreshold;
         float alpha = 1.f;
@@ -345,6 +373,10 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             m_run = m_new;
         }
         if (__any_sync(0xffffffffu, need && o_valid)) {
+            // O holds the previous tile's PV only once that MMA has finished
+            ok = wait_bar(bar_addr(sh.pv_done[h]), (gi - 1) & 1, abort, p.dev_err);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
             const float a = (need && o_valid) ? alpha : 1.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -373,24 +405,23 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             }
             fence_proxy_async_smem();
         }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        // P = 2^(s * scale * log2 e - m), packed to bf16 pairs over the first
+        // 32 columns of the S buffer
+        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float p0 = ex2(__uint_as_float(s[2 * k2 + (e >> 4)][(e & 15) * 2]) - m_use);
-                const float p1 = ex2(__uint_as_float(s[2 * k2 + (e >> 4)][(e & 15) * 2 + 1]) - m_use);
-                ls[e & 3] += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
-            }
-            tmem_st32(tS + 32 * k2, pk);
+        for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(s[e >> 4][(e & 15) * 2]), c2, neg_m));
+            const float p1 = ex2(fmaf(__uint_as_float(s[e >> 4][(e & 15) * 2 + 1]), c2, neg_m));
+            ls[e & 3] += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
         }
+        tmem_st32(tS + buf * 64, pk);
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_addr(sh.p_full[h]));
+        mbar_arrive(bar_addr(sh.p_full[h][buf]));
         o_valid = true;
 
         if (t.last) {
@@ -425,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     TcShared &sh = *reinterpret_cast<TcShared *>(smem + kOffShared);
     int32_t *lens_s = reinterpret_cast<int32_t *>(smem + kOffSched);
     int64_t *pre_s = reinterpret_cast<int64_t *>(smem + kOffSched + ((p.B * 4 + 15) / 16) * 16);
+    int64_t *lo_s = pre_s + p.B + 1;
     const uint32_t sQ = smem_u32(smem + kOffQ), ring = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5;
 
@@ -434,8 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_addr(sh.empty[s]), 1);
         }
         for (int h = 0; h < 2; ++h) {
-            mbar_init(bar_addr(sh.s_full[h]), 1);
-            mbar_init(bar_addr(sh.p_full[h]), 128);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar_addr(sh.s_full[h][b]), 1);
+                mbar_init(bar_addr(sh.p_full[h][b]), 128);
+            }
+            mbar_init(bar_addr(sh.pv_done[h]), 1);
             mbar_init(bar_addr(sh.o_done[h]), 1);
             mbar_init(bar_addr(sh.o_free[h]), 128);
             mbar_init(bar_addr(sh.q_full[h]), 128);
@@ -457,17 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before();
     }
-    build_schedule(p, lens_s, pre_s);  // ends with __syncthreads
+    build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    const int64_t U = pre_s[p.B];
-    const int64_t u0 = cta_lo(blockIdx.x, U, gridDim.x), u1 = cta_lo(blockIdx.x + 1, U, gridDim.x);
+    const int64_t u0 = lo_s[blockIdx.x], u1 = lo_s[blockIdx.x + 1];
     const int halves = (p.rows_pg + kHalf - 1) / kHalf;
 
-    // register split: 128 x 72 for the control warpgroup, 256 x 216 for the
+    // register split: 128 x 152 for the control warpgroup, 256 x 176 for the
     // softmax warpgroups (= 384 x 168 at launch); restored before the merge
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
         if (warp == 0) {
             if ((threadIdx.x & 31) == 0) producer(p, maps, sh, ring, lens_s, pre_s, u0, u1);
         } else if (warp == 1) {
@@ -475,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
         const int h = (warp >> 2) - 1;
         if (h < halves) softmax_wg(p, sh, sQ, ring, tmem, h, lens_s, pre_s, u0, u1);
         __syncwarp();
@@ -497,12 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool ok = grid_barrier(p);
     // Q and the K/V ring are idle now: they stage the merge
-    merge_phase<128>(p, lens_s, pre_s, ok, smem + kOffQ, kOffShared - kOffQ);
+    merge_phase<128>(p, lens_s, pre_s, lo_s, ok, smem + kOffQ, kOffShared - kOffQ);
     grid_barrier_depart(p);
 }
 
-size_t tc_smem_bytes(int B) {
-    return 1024 + kOffSched + sched_bytes(B);
+size_t tc_smem_bytes(int B, int grid) {
+    return 1024 + kOffSched + sched_bytes(B, grid);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -519,13 +553,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [rows][d=128] bf16 per (b, kv head), boxes of 128 rows x 64 dims, 128-byte swizzle
+// [rows][d=128] bf16 per (b, kv head), boxes of 64 rows x 64 dims, 128-byte swizzle
 bool encode_kv(CUtensorMap *map, const void *base, int64_t rows, int64_t heads) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {128, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)heads};
     const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)(rows > 0 ? rows : 1) * 128 * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -538,14 +572,14 @@ int tc_rows_per_group() { return kMaxRows; }
 int tc_tile() { return kTile; }
 
 int tc_max_grid(int B, int num_sms) {
-    const size_t smem = tc_smem_bytes(B);
+    const size_t smem = tc_smem_bytes(B, num_sms);
     if (cudaFuncSetAttribute(k_tc_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_tc_verify, kThreads, smem) != cudaSuccess)
         return 0;
-    return occ * num_sms;
+    return occ >= 1 ? num_sms : 0;  // one CTA per SM (the boundary table is sized for that)
 }
 
 cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
@@ -557,7 +591,7 @@ cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     if (p.include_tree &&
         (!encode_kv(&maps.ks, p.k_spec, p.T, heads) || !encode_kv(&maps.vs, p.v_spec, p.T, heads)))
         return cudaErrorInvalidValue;
-    const size_t smem = tc_smem_bytes(p.B);
+    const size_t smem = tc_smem_bytes(p.B, grid);
     cudaError_t e = cudaFuncSetAttribute(k_tc_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
