@@ -328,12 +328,8 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
         bool ok = wait_bar(bar_addr(sh.s_full[h][buf]), (gi >> 1) & 1, abort, p.dev_err);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        uint32_t s[2][32];
-        tmem_ld32(tS + buf * 64, s[0]);
-        tmem_ld32(tS + buf * 64 + 32, s[1]);
-        tmem_wait_ld();
-        reg_fence32(s[0]);
-        reg_fence32(s[1]);
+        uint32_t sv[64];  // raw scores of keys 0..63 of this tile
+        tmem_ld64(tS + buf * 64, sv);
 
         // raw-score max (the scale is positive); masked keys become -inf
         float mx[8];
@@ -343,7 +339,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
 #pragma unroll
             for (int k = 0; k < 2; ++k)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(s[k][e]));
+                for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sv[32 * k + e]));
         } else {
             // mask words of this tile: a tree has at most four tiles of 64 keys;
             // rows past the group see every key (their result is discarded)
@@ -358,8 +354,8 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const bool vis = (32 * k + e) < nvalid && ((w2[k] >> e) & 1u);
-                    if (!vis) s[k][e] = 0xff800000u;  // -inf
-                    mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(s[k][e]));
+                    if (!vis) sv[32 * k + e] = 0xff800000u;  // -inf
+                    mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sv[32 * k + e]));
                 }
         }
         const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -382,8 +378,6 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             for (int k = 0; k < 4; ++k) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * k, o);
-                tmem_wait_ld();
-                reg_fence32(o);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * a);
                 tmem_st32(tO + 32 * k, o);
@@ -412,8 +406,8 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[e >> 4][(e & 15) * 2]), c2, neg_m));
-            const float p1 = ex2(fmaf(__uint_as_float(s[e >> 4][(e & 15) * 2 + 1]), c2, neg_m));
+            const float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, neg_m));
+            const float p1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, neg_m));
             ls[e & 3] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
         }
@@ -433,8 +427,6 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             for (int k = 0; k < 4; ++k) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * k, o);
-                tmem_wait_ld();
-                reg_fence32(o);
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)

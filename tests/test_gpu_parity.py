@@ -141,6 +141,31 @@ def test_verify_explicit_scale(oracle_mod, path):
     assert_close(o, lse, o_ref, lse_ref, "scale 0.05")
 
 
+@pytest.mark.parametrize("path", PATHS, indirect=True)
+@pytest.mark.parametrize("scale", [1.0, 4.0])
+def test_verify_large_scale_near_one_hot(oracle_mod, path, scale):
+    """Large softmax scales make the softmax nearly one-hot and the running
+    max move by tens of units between tiles: a wrong reference max would
+    overflow, and the rescale of O runs on many tiles."""
+    inp = wl.random_inputs(2, 64, 16, 4, 128, [1500, 777], seed=29, tree="window8_depth8")
+    o, lse = run_verify(inp, path, scale=scale)
+    o_ref, lse_ref = oracle_full(oracle_mod, inp, scale=scale)
+    assert_close(o, lse, o_ref, lse_ref, f"scale {scale}")
+
+
+@pytest.mark.parametrize("path", PATHS, indirect=True)
+def test_verify_growing_keys_force_rescale(oracle_mod, path):
+    """Cache keys grow in magnitude with position, so every new tile raises
+    the running max (the O rescale path runs on most tiles)."""
+    inp = wl.random_inputs(1, 32, 8, 2, 128, [2048], seed=31)
+    kf = wl.bf16_bits_to_f32(inp.k_cache)
+    growth = (1.0 + np.arange(kf.shape[2], dtype=np.float32) / 128.0)[None, None, :, None]
+    inp.k_cache[...] = wl.f32_to_bf16_bits(np.nan_to_num(kf, nan=0.0) * growth)
+    o, lse = run_verify(inp, path)
+    o_ref, lse_ref = oracle_full(oracle_mod, inp)
+    assert_close(o, lse, o_ref, lse_ref, "growing keys")
+
+
 @pytest.mark.parametrize("path", ["cc", "tc"], indirect=True)
 def test_verify_is_deterministic(path):
     inp = wl.random_inputs(2, 64, 32, 8, 128, [3000, 1700], seed=9, tree="window8_depth8")
