@@ -168,21 +168,22 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     TileInfo t;
     uint32_t n = 0;  // ring fills issued
     bool ok = true;
+    const uint32_t leader = elect_one();
     while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int z = t.b * p.Hkv + t.kvh;
         for (int kv = 0; kv < 2; ++kv, ++n) {
             const uint32_t st = n % kStages, round = n / kStages;
-            if (!wait_bar(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err)) {
+            if (!__all_sync(0xffffffffu, wait_bar(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err))) {
                 ok = false;
                 break;
             }
             const CUtensorMap *map = tree ? (kv ? &maps.vs : &maps.ks) : (kv ? &maps.vc : &maps.kc);
             const uint32_t full = bar_addr(sh.full[st]);
-            mbar_arrive_expect_tx(full, kTileBytes);
-            tma_load_3d(ring + st * kTileBytes, map, full, 0, y, z);
-            tma_load_3d(ring + st * kTileBytes + kSubBytes, map, full, 64, y, z);
+            mbar_arrive_expect_tx_if(leader, full, kTileBytes);
+            tma_load_3d(leader, ring + st * kTileBytes, map, full, 0, y, z);
+            tma_load_3d(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z);
         }
     }
     if (!ok) {
@@ -205,6 +206,11 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     volatile int32_t *abort = &sh.abort;
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
+    const uint32_t leader = elect_one();
+    // every lane waits; the warp leaves together if any lane gives up
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, p.dev_err));
+    };
     Cursor c;
     cursor_init(c, u0, u1);
     TileInfo cur, n1, n2;
@@ -215,17 +221,17 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     // S(h,j) = Q_h K(j)^T into S buffer j&1 of half h
     auto issue_s = [&](int h, uint32_t j, const TileInfo &tj) -> bool {
         const uint32_t n = 2 * j, st = n % kStages, round = n / kStages;
-        if (h == 0 && !wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return false;
-        if (tj.first && !wait_bar(bar_addr(sh.q_full[h]), tj.q & 1, abort, p.dev_err)) return false;
+        if (h == 0 && !wait_all(bar_addr(sh.full[st]), round & 1)) return false;
+        if (tj.first && !wait_all(bar_addr(sh.q_full[h]), tj.q & 1)) return false;
         tc_fence_after();
         const uint32_t qa = sQ + h * kQHalfBytes, kb = ring + st * kTileBytes;
         const uint32_t d = tmem + h * 128 + (j & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_ss(d, smem_desc_sw128(qa + (kk >> 2) * kQSubBytes + (kk & 3) * 32, 16, 1024),
+            mma_ss(leader, d, smem_desc_sw128(qa + (kk >> 2) * kQSubBytes + (kk & 3) * 32, 16, 1024),
                    smem_desc_sw128(kb + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
-        mma_commit(bar_addr(sh.s_full[h][j & 1]));
-        if (h == halves - 1) mma_commit(bar_addr(sh.empty[st]));
+        mma_commit(leader, bar_addr(sh.s_full[h][j & 1]));
+        if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[st]));
         return true;
     };
 
@@ -236,22 +242,20 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             if (!issue_s(h, 1, n1)) return;
     for (uint32_t i = 0;; ++i) {
         const uint32_t nv = 2 * i + 1, stv = nv % kStages, rv = nv / kStages;
-        if (!wait_bar(bar_addr(sh.full[stv]), rv & 1, abort, p.dev_err)) return;
+        if (!wait_all(bar_addr(sh.full[stv]), rv & 1)) return;
         const uint32_t vb = ring + stv * kTileBytes;
         for (int h = 0; h < halves; ++h) {
-            if (!wait_bar(bar_addr(sh.p_full[h][i & 1]), (i >> 1) & 1, abort, p.dev_err)) return;
-            if (cur.first && cur.q > 0 &&
-                !wait_bar(bar_addr(sh.o_free[h]), (cur.q - 1) & 1, abort, p.dev_err))
-                return;
+            if (!wait_all(bar_addr(sh.p_full[h][i & 1]), (i >> 1) & 1)) return;
+            if (cur.first && cur.q > 0 && !wait_all(bar_addr(sh.o_free[h]), (cur.q - 1) & 1)) return;
             tc_fence_after();
             const uint32_t pa = tmem + h * 128 + (i & 1) * 64;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColO + h * 128, pa + kk * 8, smem_desc_sw128(vb + kk * 2048, kSubBytes, 1024),
+                mma_ts(leader, tmem + kColO + h * 128, pa + kk * 8, smem_desc_sw128(vb + kk * 2048, kSubBytes, 1024),
                        idesc_pv, (!cur.first || kk > 0) ? 1u : 0u);
-            mma_commit(bar_addr(sh.pv_done[h]));
-            if (h == halves - 1) mma_commit(bar_addr(sh.empty[stv]));
-            if (cur.last) mma_commit(bar_addr(sh.o_done[h]));
+            mma_commit(leader, bar_addr(sh.pv_done[h]));
+            if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[stv]));
+            if (cur.last) mma_commit(leader, bar_addr(sh.o_done[h]));
             if (has1 && n1.first && !issue_s(h, i + 1, n1)) return;
             if (has2 && !n2.first && !issue_s(h, i + 2, n2)) return;
         }
@@ -494,11 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax warpgroups (= 384 x 168 at launch); restored before the merge
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
-        if (warp == 0) {
-            if ((threadIdx.x & 31) == 0) producer(p, maps, sh, ring, lens_s, pre_s, u0, u1);
-        } else if (warp == 1) {
-            if ((threadIdx.x & 31) == 0) mma_issuer(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
-        }
+        if (warp == 0)
+            producer(p, maps, sh, ring, lens_s, pre_s, u0, u1);
+        else if (warp == 1)
+            mma_issuer(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
         __syncwarp();
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
@@ -510,13 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp < 4) asm volatile("setmaxnreg.inc.sync.aligned.u32 168;");
     if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) {
-            // every MMA of this CTA has finished before tensor memory is freed
-            mma_commit(bar_addr(sh.drain));
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar_addr(sh.drain), 0))
-                if (globaltimer_ns() - t0 > kTimeoutNs) break;
-        }
+        // every MMA of this CTA has finished before tensor memory is freed
+        mma_commit(elect_one(), bar_addr(sh.drain));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar_addr(sh.drain), 0))
+            if (globaltimer_ns() - t0 > kTimeoutNs) break;
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
