@@ -29,7 +29,7 @@ TMAX, BMAX = 256, 1024
 
 # every exported symbol of include/hta.h
 EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
-           "hta_merge", "hta_verify", "hta_status_string", "hta_last_path")
+           "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_status_string", "hta_last_path")
 
 
 class HtaError(RuntimeError):
@@ -68,10 +68,12 @@ def load():
         lib.hta_tree_attn.argtypes = [D, P, P, P, P, P, P, P]
         lib.hta_merge.argtypes = [D, P, P, P, P, P, P, P]
         lib.hta_verify.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+        lib.hta_verify_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_status_string.argtypes = [ctypes.c_int]
         lib.hta_status_string.restype = ctypes.c_char_p
         lib.hta_last_path.restype = I32
-        for name in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge", "hta_verify"):
+        for name in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge", "hta_verify",
+                     "hta_verify_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
