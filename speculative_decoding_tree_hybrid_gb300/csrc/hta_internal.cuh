@@ -70,6 +70,11 @@ __device__ __forceinline__ void flag_error(int32_t *dev_err, int32_t f) {
     if (dev_err) atomicOr(dev_err, f);
 }
 
+// SM cycle counter: cheap to read, used to bound every wait (a read of the
+// global timer costs far more and would sit on the hot wait paths)
+__device__ __forceinline__ uint64_t cycles_now() { return (uint64_t)clock64(); }
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;  // ~2 s at 2 GHz
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -200,13 +205,13 @@ __device__ inline bool grid_barrier(const AttnParams &p) {
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(&p.bar[0], 1u);
-        const uint64_t t0 = globaltimer_ns();
+        const uint64_t t0 = cycles_now();
         int ok = 1;
         unsigned int v;
         for (;;) {
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.bar) : "memory");
             if (v >= gridDim.x) break;
-            if (globaltimer_ns() - t0 > 2000000000ull) {
+            if (cycles_now() - t0 > 2 * kWaitLimitCycles) {
                 ok = 0;
                 flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
                 break;
@@ -315,9 +320,9 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                     const float *src = p.ws_rec + (slot_of(seg, c) * p.rows_pg + lr_a) * REC;
                     tc::bulk_load(tc::smem_u32(buf + (uint32_t)k * nr * REC_BYTES), src, nr * REC_BYTES, bar);
                 }
-                const uint64_t t0 = globaltimer_ns();
+                const uint64_t t0 = cycles_now();
                 while (!tc::mbar_try_wait(bar, phase)) {
-                    if (globaltimer_ns() - t0 > 1000000000ull) {
+                    if (cycles_now() - t0 > kWaitLimitCycles) {
                         ok = 0;
                         flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
                         break;

@@ -4,7 +4,7 @@
 // Efficient Drafting and Verification", Korean summary section 2.C, Dutch
 // summary Methodologie section 3) splits the verification attention into an
 // unmasked pass over the long cached prefix and a masked pass over the tree
-// tokens, merged by log-sum-exp. Here both passes are 64-key tiles of one
+// tokens, merged by log-sum-exp. Here both passes are 128-key tiles of one
 // persistent cooperative grid (one CTA per SM, a static split-KV schedule
 // balanced by tile count, see hta_internal.cuh), and the cross-split and
 // cross-part merge runs after a grid barrier in the same launch.
@@ -12,27 +12,27 @@
 // One CTA works on a row group of up to 256 packed query rows of one KV head
 // (row r = t*G + g, so every K/V tile is shared by all G query heads of the
 // tree), as two 128-row halves:
-//   warp 0        TMA producer: K and V tiles (64 keys x 128 dims, bf16,
-//                 128-byte swizzle) into a 9-stage shared-memory ring;
-//   warp 1        MMA issuer (one thread): S(h,i) = Q_h K(i)^T into tensor
-//                 memory, then O_h += P(h,i) V(i) with P read from tensor memory;
+//   warp 0        TMA producer: K and V tiles (128 keys x 128 dims, bf16,
+//                 128-byte swizzle) into a shared-memory ring;
+//   warp 1        MMA issuer: S_h = Q_h K(i)^T into tensor memory, then
+//                 O_h += P_h V(i) with P read from tensor memory;
 //   warps 4-7     softmax of half 0, one query row per thread;
 //   warps 8-11    softmax of half 1.
-// Tensor memory (512 columns): S(0,even) | S(0,odd) | S(1,even) | S(1,odd),
-// 64 columns each, then O_0 | O_1, 128 columns each. P(h,i) (bf16) overwrites
-// the first 32 columns of its S buffer. With two S buffers per half the
-// tensor core computes S(h,i+1) while the softmax works on S(h,i); the MMA
-// thread issues PV(h,i) and then S(h,i+2) into the buffer PV(h,i) reads,
-// which is safe because tensor-core operations of one thread run in issue
-// order.
-// The softmax keeps the row max in base 2 (scores times scale*log2 e) and
-// rescales O in tensor memory only when the max grows by more than 8
-// (factor 256); numerator and denominator share the stale max, so the result
-// is exact.
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each; P_h
+// (bf16) overwrites the first 64 columns of S_h. The MMA warp issues
+// PV(0,i), S(0,i+1), PV(1,i), S(1,i+1): while the softmax of one half works,
+// the tensor core runs the other half's products. Tensor-core operations of
+// one thread execute in issue order, so S(h,i+1) never overtakes PV(h,i)
+// that still reads P_h, and the arrival of S(h,i) implies PV(h,i-1) is done
+// (the softmax may then rescale O_h). The softmax keeps the row max in base 2
+// (scores times scale*log2 e) and rescales O only when the max grows by more
+// than 8 (factor 256); numerator and denominator share the stale max, so the
+// result is exact.
 //
-// Every wait is bounded (~1 s of device time); on expiry the kernel sets
-// HTA_DEVERR_TIMEOUT, waits for its own copies in flight, frees its tensor
-// memory and finishes instead of hanging.
+// Producer and MMA warps run their loops warp-uniformly; one elected lane
+// issues each TMA / MMA / commit. Every wait is bounded (~4e9 SM cycles,
+// about 2 s); on expiry the kernel sets HTA_DEVERR_TIMEOUT, waits for its own
+// copies in flight, frees its tensor memory and finishes instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,34 +46,35 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTile = 64;           // keys per tile
+constexpr int kTile = 128;          // keys per tile
 constexpr int kHalf = 128;          // query rows per MMA
 constexpr int kMaxRows = 256;       // rows per row group
-constexpr int kStages = 9;          // K/V ring stages
 constexpr int kThreads = 384;
-constexpr uint32_t kTileBytes = 64 * 128 * 2;    // one K or V tile
-constexpr uint32_t kSubBytes = 64 * 64 * 2;      // one 64-dim swizzled sub-tile of it
+constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one K or V tile
+constexpr uint32_t kSubBytes = 128 * 64 * 2;     // one 64-dim swizzled sub-tile of it
 constexpr uint32_t kQHalfBytes = 128 * 128 * 2;  // Q rows of one half
 constexpr uint32_t kQSubBytes = 128 * 64 * 2;    // one 64-dim sub-tile of them
+constexpr int kMaxStages = 5;                    // K/V ring stages (4 when the schedule is large)
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = 2 * kQHalfBytes;
-constexpr uint32_t kOffShared = kOffRing + kStages * kTileBytes;
 constexpr uint32_t kSharedBytes = 512;
-constexpr uint32_t kOffSched = kOffShared + kSharedBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;     // S buffers take columns 0..255
-constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr uint32_t kColO = 256;  // S_0, S_1 take columns 0..255
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
+
+__host__ __device__ constexpr uint32_t off_shared(int stages) { return kOffRing + stages * kTileBytes; }
+__host__ __device__ constexpr uint32_t off_sched(int stages) { return off_shared(stages) + kSharedBytes; }
 
 struct TcMaps {
     CUtensorMap kc, vc, ks, vs;
 };
 
 struct TcShared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t s_full[2][2], p_full[2][2];  // [half][S buffer]
-    uint64_t pv_done[2], o_done[2], o_free[2], q_full[2];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2], q_full[2];
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -87,16 +88,20 @@ __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_u3
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort,
                                          int32_t *dev_err) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = cycles_now();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kTimeoutNs) {
+        if (cycles_now() - t0 > kWaitLimitCycles) {
             *abort = 1;
             flag_error(dev_err, HTA_DEVERR_TIMEOUT);
             return false;
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *dev_err) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, dev_err));
 }
 
 // Walks the CTA's unit range tile by tile, piece by piece.
@@ -159,6 +164,7 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const AttnParams &p, cons
 
 // ------------------------------------------------------------------ roles
 
+template <int kStages>
 __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, uint32_t ring,
                          const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
@@ -169,104 +175,113 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     uint32_t n = 0;  // ring fills issued
     bool ok = true;
     const uint32_t leader = elect_one();
+    // K and V are streamed once: keep them from evicting everything else in L2
+    const uint64_t policy = l2_evict_first_policy();
     while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int z = t.b * p.Hkv + t.kvh;
         for (int kv = 0; kv < 2; ++kv, ++n) {
             const uint32_t st = n % kStages, round = n / kStages;
-            if (!__all_sync(0xffffffffu, wait_bar(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err))) {
+            if (!wait_warp(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err)) {
                 ok = false;
                 break;
             }
             const CUtensorMap *map = tree ? (kv ? &maps.vs : &maps.ks) : (kv ? &maps.vc : &maps.kc);
             const uint32_t full = bar_addr(sh.full[st]);
             mbar_arrive_expect_tx_if(leader, full, kTileBytes);
-            tma_load_3d(leader, ring + st * kTileBytes, map, full, 0, y, z);
-            tma_load_3d(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z);
+            tma_load_3d_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, policy);
+            tma_load_3d_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, policy);
         }
     }
     if (!ok) {
         // let the copies already issued land before the CTA exits
-        const uint64_t t0 = globaltimer_ns();
+        const uint64_t t0 = cycles_now();
         for (uint32_t k = n > (uint32_t)kStages ? n - kStages : 0; k < n; ++k) {
             const uint32_t st = k % kStages, round = k / kStages;
             while (!mbar_try_wait(bar_addr(sh.full[st]), round & 1))
-                if (globaltimer_ns() - t0 > kTimeoutNs) break;
+                if (cycles_now() - t0 > kWaitLimitCycles) break;
         }
     }
 }
 
-// Issue order per half: S(0), S(1), PV(0), S(2), PV(1), S(3), ... where the
-// first tile of a piece waits for the previous tile's PV instead (its Q is
-// loaded only after the previous piece's output was read). The two halves
-// alternate op by op.
+// 8 MMAs over d = 128: S_h[128 x 128] = Q_h[128 x 128] K^T
+__device__ __forceinline__ void issue_qk(uint32_t leader, uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t o = ((kk >> 2) * kSubBytes + (kk & 3) * 32) >> 4;  // same layout for Q and K
+        mma_ss(leader, d_tmem, q_desc + o, k_desc + o, kIdescQK, kk > 0);
+    }
+}
+
+// 8 MMAs over 128 keys: O_h[128 x 128] (+)= P_h[128 x 128] V[128 x 128]
+__device__ __forceinline__ void issue_pv(uint32_t leader, uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                         bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ts(leader, o_tmem, p_tmem + kk * 8, v_desc + ((kk * 2048) >> 4), kIdescPV,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// S(h,j): waits for K(j) (on the first half) and, at the start of a piece,
+// for the half's Q rows
+template <int kStages>
+__device__ __forceinline__ bool issue_s_tile(const AttnParams &p, TcShared &sh, volatile int32_t *abort,
+                                             uint32_t leader, int h, int halves, uint32_t j, bool first, int32_t q,
+                                             uint32_t tmem, uint64_t q_desc0, uint64_t k_desc0) {
+    const uint32_t n = 2 * j, st = n % kStages, round = n / kStages;
+    if (h == 0 && !wait_warp(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return false;
+    if (first && !wait_warp(bar_addr(sh.q_full[h]), q & 1, abort, p.dev_err)) return false;
+    tc_fence_after();
+    issue_qk(leader, tmem + h * 128, q_desc0 + ((h * kQHalfBytes) >> 4), k_desc0 + ((st * kTileBytes) >> 4));
+    mma_commit(leader, bar_addr(sh.s_full[h]));
+    if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[st]));
+    return true;
+}
+
+// Issue order: S(0,0), S(1,0), then per tile i: PV(0,i), S(0,i+1), PV(1,i),
+// S(1,i+1). The first S of a piece waits for that half's new Q rows, which
+// the softmax loads only after reading out the previous piece's O.
+template <int kStages>
 __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
                            int halves, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, 0, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
     const uint32_t leader = elect_one();
-    // every lane waits; the warp leaves together if any lane gives up
-    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, p.dev_err));
-    };
+    const uint64_t q_desc0 = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t k_desc0 = smem_desc_sw128(ring, 16, 1024);
+    const uint64_t v_desc0 = smem_desc_sw128(ring, kSubBytes, 1024);
     Cursor c;
     cursor_init(c, u0, u1);
-    TileInfo cur, n1, n2;
+    TileInfo cur, nxt;
     if (!cursor_next(c, p, lens_s, pre_s, cur)) return;
-    bool has1 = cursor_next(c, p, lens_s, pre_s, n1);
-    bool has2 = has1 && cursor_next(c, p, lens_s, pre_s, n2);
-
-    // S(h,j) = Q_h K(j)^T into S buffer j&1 of half h
-    auto issue_s = [&](int h, uint32_t j, const TileInfo &tj) -> bool {
-        const uint32_t n = 2 * j, st = n % kStages, round = n / kStages;
-        if (h == 0 && !wait_all(bar_addr(sh.full[st]), round & 1)) return false;
-        if (tj.first && !wait_all(bar_addr(sh.q_full[h]), tj.q & 1)) return false;
-        tc_fence_after();
-        const uint32_t qa = sQ + h * kQHalfBytes, kb = ring + st * kTileBytes;
-        const uint32_t d = tmem + h * 128 + (j & 1) * 64;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_ss(leader, d, smem_desc_sw128(qa + (kk >> 2) * kQSubBytes + (kk & 3) * 32, 16, 1024),
-                   smem_desc_sw128(kb + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024), idesc_qk, kk > 0);
-        mma_commit(leader, bar_addr(sh.s_full[h][j & 1]));
-        if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[st]));
-        return true;
-    };
+    bool has_next = cursor_next(c, p, lens_s, pre_s, nxt);
 
     for (int h = 0; h < halves; ++h)
-        if (!issue_s(h, 0, cur)) return;
-    if (has1 && !n1.first)
-        for (int h = 0; h < halves; ++h)
-            if (!issue_s(h, 1, n1)) return;
+        if (!issue_s_tile<kStages>(p, sh, abort, leader, h, halves, 0, cur.first, cur.q, tmem, q_desc0, k_desc0))
+            return;
     for (uint32_t i = 0;; ++i) {
         const uint32_t nv = 2 * i + 1, stv = nv % kStages, rv = nv / kStages;
-        if (!wait_all(bar_addr(sh.full[stv]), rv & 1)) return;
-        const uint32_t vb = ring + stv * kTileBytes;
+        if (!wait_warp(bar_addr(sh.full[stv]), rv & 1, abort, p.dev_err)) return;
+        const uint64_t v_desc = v_desc0 + ((stv * kTileBytes) >> 4);
         for (int h = 0; h < halves; ++h) {
-            if (!wait_all(bar_addr(sh.p_full[h][i & 1]), (i >> 1) & 1)) return;
-            if (cur.first && cur.q > 0 && !wait_all(bar_addr(sh.o_free[h]), (cur.q - 1) & 1)) return;
+            if (!wait_warp(bar_addr(sh.p_full[h]), i & 1, abort, p.dev_err)) return;
+            if (cur.first && cur.q > 0 && !wait_warp(bar_addr(sh.o_free[h]), (cur.q - 1) & 1, abort, p.dev_err))
+                return;
             tc_fence_after();
-            const uint32_t pa = tmem + h * 128 + (i & 1) * 64;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_ts(leader, tmem + kColO + h * 128, pa + kk * 8, smem_desc_sw128(vb + kk * 2048, kSubBytes, 1024),
-                       idesc_pv, (!cur.first || kk > 0) ? 1u : 0u);
-            mma_commit(leader, bar_addr(sh.pv_done[h]));
+            issue_pv(leader, tmem + kColO + h * 128, tmem + h * 128, v_desc, !cur.first);
             if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[stv]));
             if (cur.last) mma_commit(leader, bar_addr(sh.o_done[h]));
-            if (has1 && n1.first && !issue_s(h, i + 1, n1)) return;
-            if (has2 && !n2.first && !issue_s(h, i + 2, n2)) return;
+            if (has_next && !issue_s_tile<kStages>(p, sh, abort, leader, h, halves, i + 1, nxt.first, nxt.q, tmem,
+                                                   q_desc0, k_desc0))
+                return;
         }
-        if (!has1) break;
-        cur = n1;
-        has1 = has2;
-        n1 = n2;
-        has2 = has2 && cursor_next(c, p, lens_s, pre_s, n2);
+        if (!has_next) break;
+        cur = nxt;
+        has_next = cursor_next(c, p, lens_s, pre_s, nxt);
     }
 }
 
+template <int kStages>
 __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
                            int h, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
@@ -274,7 +289,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     const int row = wq * 32 + lane;  // row of this half == TMEM lane
     const int tid_wg = threadIdx.x & 127;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + h * 128;  // + 64 for the odd S buffer
+    const uint32_t tS = tmem + lane_off + h * 128;
     const uint32_t tO = tmem + lane_off + kColO + h * 128;
     const int n_tree = p.include_tree ? p.n_tree_tiles : 0;
     const float c2 = p.scale_log2;
@@ -327,13 +342,13 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
         const bool tree = t.unit < n_tree;
         const int j0 = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int nvalid = tree ? min(kTile, p.T - j0) : min(kTile, t.Lb - j0);
-        const uint32_t buf = gi & 1;
 
-        bool ok = wait_bar(bar_addr(sh.s_full[h][buf]), (gi >> 1) & 1, abort, p.dev_err);
+        bool ok = wait_bar(bar_addr(sh.s_full[h]), gi & 1, abort, p.dev_err);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        uint32_t sv[64];  // raw scores of keys 0..63 of this tile
-        tmem_ld64(tS + buf * 64, sv);
+        uint32_t sa[64], sb[64];  // raw scores of keys 0..63 and 64..127
+        tmem_ld64(tS, sa);
+        tmem_ld64(tS + 64, sb);
 
         // raw-score max (the scale is positive); masked keys become -inf
         float mx[8];
@@ -341,26 +356,26 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
         for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
         if (!tree && nvalid == kTile) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sv[32 * k + e]));
-        } else {
-            // mask words of this tile: a tree has at most four tiles of 64 keys;
-            // rows past the group see every key (their result is discarded)
-            uint32_t w2[2];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const uint32_t w = t.unit == 0 ? mw[k] : t.unit == 1 ? mw[2 + k] : t.unit == 2 ? mw[4 + k] : mw[6 + k];
-                w2[k] = (tree && valid) ? w : 0xffffffffu;
+            for (int e = 0; e < 64; ++e) {
+                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sa[e]));
+                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sb[e]));
             }
+        } else {
+            // mask words of this tile (a tree has at most two tiles of 128
+            // keys); rows past the group see every key (their result is
+            // discarded)
+            uint32_t w4[4];
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
+            for (int k = 0; k < 4; ++k) w4[k] = (tree && valid) ? (t.unit == 0 ? mw[k] : mw[4 + k]) : 0xffffffffu;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const bool vis = (32 * k + e) < nvalid && ((w2[k] >> e) & 1u);
-                    if (!vis) sv[32 * k + e] = 0xff800000u;  // -inf
-                    mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sv[32 * k + e]));
-                }
+            for (int e = 0; e < 64; ++e) {
+                const bool va = e < nvalid && ((w4[e >> 5] >> (e & 31)) & 1u);
+                const bool vb = (e + 64) < nvalid && ((w4[2 + (e >> 5)] >> (e & 31)) & 1u);
+                if (!va) sa[e] = 0xff800000u;  // -inf
+                if (!vb) sb[e] = 0xff800000u;
+                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sa[e]));
+                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sb[e]));
+            }
         }
         const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c2;
@@ -373,12 +388,9 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             m_run = m_new;
         }
         if (__any_sync(0xffffffffu, need && o_valid)) {
-            // O holds the previous tile's PV only once that MMA has finished
-            ok = wait_bar(bar_addr(sh.pv_done[h]), (gi - 1) & 1, abort, p.dev_err);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
+            // S_h arrived after PV(h, previous tile) finished: O_h is stable
             const float a = (need && o_valid) ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
             for (int k = 0; k < 4; ++k) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * k, o);
@@ -404,22 +416,35 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             fence_proxy_async_smem();
         }
         // P = 2^(s * scale * log2 e - m), packed to bf16 pairs over the first
-        // 32 columns of the S buffer
+        // 64 columns of S_h (all of S_h is already in registers)
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
+        {
+            uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, neg_m));
-            const float p1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, neg_m));
-            ls[e & 3] += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2(fmaf(__uint_as_float(sa[2 * e]), c2, neg_m));
+                const float p1 = ex2(fmaf(__uint_as_float(sa[2 * e + 1]), c2, neg_m));
+                ls[e & 3] += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS, pk);
         }
-        tmem_st32(tS + buf * 64, pk);
+        {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2(fmaf(__uint_as_float(sb[2 * e]), c2, neg_m));
+                const float p1 = ex2(fmaf(__uint_as_float(sb[2 * e + 1]), c2, neg_m));
+                ls[e & 3] += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS + 32, pk);
+        }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_addr(sh.p_full[h][buf]));
+        mbar_arrive(bar_addr(sh.p_full[h]));
         o_valid = true;
 
         if (t.last) {
@@ -427,7 +452,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             float *rec = p.ws_rec + (slot_of(t.seg, blockIdx.x) * p.rows_pg + r_local) * 132;
-#pragma unroll
+#pragma unroll 1
             for (int k = 0; k < 4; ++k) {
                 uint32_t o[32];
                 tmem_ld32(tO + 32 * k, o);
@@ -445,13 +470,14 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     }
 }
 
+template <int kStages>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_verify(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    TcShared &sh = *reinterpret_cast<TcShared *>(smem + kOffShared);
-    int32_t *lens_s = reinterpret_cast<int32_t *>(smem + kOffSched);
-    int64_t *pre_s = reinterpret_cast<int64_t *>(smem + kOffSched + ((p.B * 4 + 15) / 16) * 16);
+    TcShared &sh = *reinterpret_cast<TcShared *>(smem + off_shared(kStages));
+    int32_t *lens_s = reinterpret_cast<int32_t *>(smem + off_sched(kStages));
+    int64_t *pre_s = reinterpret_cast<int64_t *>(smem + off_sched(kStages) + ((p.B * 4 + 15) / 16) * 16);
     int64_t *lo_s = pre_s + p.B + 1;
     const uint32_t sQ = smem_u32(smem + kOffQ), ring = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5;
@@ -462,11 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_addr(sh.empty[s]), 1);
         }
         for (int h = 0; h < 2; ++h) {
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(bar_addr(sh.s_full[h][b]), 1);
-                mbar_init(bar_addr(sh.p_full[h][b]), 128);
-            }
-            mbar_init(bar_addr(sh.pv_done[h]), 1);
+            mbar_init(bar_addr(sh.s_full[h]), 1);
+            mbar_init(bar_addr(sh.p_full[h]), 128);
             mbar_init(bar_addr(sh.o_done[h]), 1);
             mbar_init(bar_addr(sh.o_free[h]), 128);
             mbar_init(bar_addr(sh.q_full[h]), 128);
@@ -494,19 +517,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u0 = lo_s[blockIdx.x], u1 = lo_s[blockIdx.x + 1];
     const int halves = (p.rows_pg + kHalf - 1) / kHalf;
 
-    // register split: 128 x 152 for the control warpgroup, 256 x 176 for the
+    // register split: 128 x 88 for the control warpgroup, 256 x 208 for the
     // softmax warpgroups (= 384 x 168 at launch); restored before the merge
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
         if (warp == 0)
-            producer(p, maps, sh, ring, lens_s, pre_s, u0, u1);
+            producer<kStages>(p, maps, sh, ring, lens_s, pre_s, u0, u1);
         else if (warp == 1)
-            mma_issuer(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
+            mma_issuer<kStages>(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
         __syncwarp();
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;");
         const int h = (warp >> 2) - 1;
-        if (h < halves) softmax_wg(p, sh, sQ, ring, tmem, h, lens_s, pre_s, u0, u1);
+        if (h < halves) softmax_wg<kStages>(p, sh, sQ, ring, tmem, h, lens_s, pre_s, u0, u1);
         __syncwarp();
         asm volatile("setmaxnreg.dec.sync.aligned.u32 168;");
     }
@@ -515,21 +538,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         // every MMA of this CTA has finished before tensor memory is freed
         mma_commit(elect_one(), bar_addr(sh.drain));
-        const uint64_t t0 = globaltimer_ns();
+        const uint64_t t0 = cycles_now();
         while (!mbar_try_wait(bar_addr(sh.drain), 0))
-            if (globaltimer_ns() - t0 > kTimeoutNs) break;
+            if (cycles_now() - t0 > kWaitLimitCycles) break;
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
     const bool ok = grid_barrier(p);
     // Q and the K/V ring are idle now: they stage the merge
-    merge_phase<128>(p, lens_s, pre_s, lo_s, ok, smem + kOffQ, kOffShared - kOffQ);
+    merge_phase<128>(p, lens_s, pre_s, lo_s, ok, smem + kOffQ, off_shared(kStages) - kOffQ);
     grid_barrier_depart(p);
 }
 
-size_t tc_smem_bytes(int B, int grid) {
-    return 1024 + kOffSched + sched_bytes(B, grid);
+size_t tc_smem_bytes(int stages, int B, int grid) {
+    return 1024 + off_sched(stages) + sched_bytes(B, grid);
+}
+
+// Deepest ring that fits next to the schedule arrays of this batch
+int tc_stages(int B, int grid) {
+    int max_smem = 0, dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    // static shared memory of the merge and barrier helpers
+    const size_t slack = 256;
+    if (tc_smem_bytes(5, B, grid) + slack <= (size_t)max_smem) return 5;
+    if (tc_smem_bytes(4, B, grid) + slack <= (size_t)max_smem) return 4;
+    return 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -546,7 +581,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [rows][d=128] bf16 per (b, kv head), boxes of 64 rows x 64 dims, 128-byte swizzle
+// [rows][d=128] bf16 per (b, kv head), boxes of 128 rows x 64 dims, 128-byte swizzle
 bool encode_kv(CUtensorMap *map, const void *base, int64_t rows, int64_t heads) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -559,19 +594,43 @@ bool encode_kv(CUtensorMap *map, const void *base, int64_t rows, int64_t heads) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int kStages>
+cudaError_t launch_stages(const AttnParams &p, const TcMaps &maps, int grid, cudaStream_t stream) {
+    const size_t smem = tc_smem_bytes(kStages, p.B, grid);
+    cudaError_t e = cudaFuncSetAttribute(k_tc_verify<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_tc_verify<kStages>, p, maps);
+}
+
 }  // namespace
 
 int tc_rows_per_group() { return kMaxRows; }
 int tc_tile() { return kTile; }
 
 int tc_max_grid(int B, int num_sms) {
-    const size_t smem = tc_smem_bytes(B, num_sms);
-    if (cudaFuncSetAttribute(k_tc_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return 0;
+    const int stages = tc_stages(B, num_sms);
+    if (stages == 0) return 0;
+    const size_t smem = tc_smem_bytes(stages, B, num_sms);
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_tc_verify, kThreads, smem) != cudaSuccess)
-        return 0;
+    if (stages == 5) {
+        if (cudaFuncSetAttribute(k_tc_verify<5>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_tc_verify<5>, kThreads, smem) != cudaSuccess)
+            return 0;
+    } else {
+        if (cudaFuncSetAttribute(k_tc_verify<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_tc_verify<4>, kThreads, smem) != cudaSuccess)
+            return 0;
+    }
     return occ >= 1 ? num_sms : 0;  // one CTA per SM (the boundary table is sized for that)
 }
 
@@ -584,20 +643,10 @@ cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     if (p.include_tree &&
         (!encode_kv(&maps.ks, p.k_spec, p.T, heads) || !encode_kv(&maps.vs, p.v_spec, p.T, heads)))
         return cudaErrorInvalidValue;
-    const size_t smem = tc_smem_bytes(p.B, grid);
-    cudaError_t e = cudaFuncSetAttribute(k_tc_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_tc_verify, p, maps);
+    const int stages = tc_stages(p.B, grid);
+    if (stages == 5) return launch_stages<5>(p, maps, grid, stream);
+    if (stages == 4) return launch_stages<4>(p, maps, grid, stream);
+    return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace hta

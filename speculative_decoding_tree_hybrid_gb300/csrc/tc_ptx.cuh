@@ -95,6 +95,27 @@ __device__ __forceinline__ void tma_load_3d(uint32_t leader, uint32_t dst, const
         : "memory");
 }
 
+// L2 policy for data read once: its lines are the first to be replaced, so
+// a stream larger than L2 does not push out code, partial results or the
+// small inputs that are read again later.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_3d with an L2 cache policy (see l2_evict_first_policy)
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t leader, uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int x, int y, int z, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%1], [%2, {%4, %5, %6}], [%3], %7;\n\t}" ::"r"(leader),
+        "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
