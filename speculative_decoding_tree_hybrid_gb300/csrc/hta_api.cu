@@ -131,6 +131,9 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
     Layout L0 = make_layout(d, path, 0, use_tree);
     const int64_t max_units =
         L0.n_seg * (int64_t)(L0.n_tree_tiles + (use_cache ? (d->Lmax + L0.tile - 1) / L0.tile : 0));
+    // the kernels index units and output rows with 32-bit arithmetic
+    if (max_units > (int64_t)0x7fffffff || L0.n_seg * (int64_t)L0.rows_pg > (int64_t)0x7fffffff)
+        return HTA_ERR_UNSUPPORTED;
     int grid;
     if (direct)
         grid = (int)(L0.n_seg < (int64_t)gmax ? L0.n_seg : gmax);

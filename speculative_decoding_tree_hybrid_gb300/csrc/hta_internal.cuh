@@ -245,29 +245,29 @@ __device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return se
 // ---------------------------------------------------------------- merge phase
 
 // Merges every output row handled by this CTA. Rows are the packed rows of
-// all segments, linearised segment-major and split evenly over the grid. The
-// CTA walks its slice in chunks of consecutive rows of one segment: thread 0
-// bulk-copies the records of those rows from every piece of the segment into
-// `buf` (one copy per piece, all in flight together), then one warp per row
-// reduces them: M = max_k m_k, w_k = 2^(m_k - M), O = sum_k w_k O_k /
-// sum_k w_k l_k, LSE = (M + log2 sum_k w_k l_k) ln 2.
+// all segments, linearised segment-major and split evenly over the grid
+// (the host keeps every row and unit count below 2^31, so 32-bit index math
+// is exact). The CTA walks its slice in chunks of consecutive rows of one
+// segment: the lanes of warp 0 bulk-copy the records of those rows from every
+// piece of the segment into `buf` (one copy per piece, all in flight
+// together), then one warp per row reduces them:
+//   M = max_k m_k, w_k = 2^(m_k - M), O = sum_k w_k O_k / sum_k w_k l_k,
+//   LSE = (M + log2 sum_k w_k l_k) ln 2.
 template <int D>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
                                    const int64_t *lo_s, bool barrier_ok, uint8_t *buf, uint32_t buf_bytes) {
-    constexpr int CPL = D / 32;        // columns per lane
-    constexpr int REC = D + 4;         // floats per record
+    constexpr int CPL = D / 32;  // columns per lane
+    constexpr int REC = D + 4;   // floats per record
     constexpr uint32_t REC_BYTES = REC * 4;
     __shared__ __align__(8) uint64_t mbar;
     __shared__ int32_t ok_s;
-    const int64_t n_seg = (int64_t)p.B * p.Hkv * p.n_rg;
-    const int64_t rows_total = n_seg * p.rows_pg;
-    const int32_t grid = gridDim.x;
-    const int64_t r0 = (blockIdx.x * rows_total) / grid;
-    const int64_t r1 = ((blockIdx.x + 1) * rows_total) / grid;
+    const uint32_t grid = gridDim.x;
+    const uint32_t rows_pg = (uint32_t)p.rows_pg, n_rg = (uint32_t)p.n_rg, hkv = (uint32_t)p.Hkv;
+    const uint32_t rows_total = (uint32_t)p.B * hkv * n_rg * rows_pg;
+    const uint32_t r0 = (uint32_t)(((uint64_t)blockIdx.x * rows_total) / grid);
+    const uint32_t r1 = (uint32_t)(((uint64_t)(blockIdx.x + 1) * rows_total) / grid);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const uint32_t bar = tc::smem_u32(&mbar);
-    // a piece exists for every CTA whose unit range is not empty
-    auto has_units = [&](int64_t c) { return lo_s[c] != lo_s[c + 1]; };
     if (threadIdx.x == 0) {
         tc::mbar_init(bar, 1);
         tc::mbar_fence_init();
@@ -275,51 +275,50 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
     __syncthreads();
     uint32_t phase = 0;
 
-    int64_t rr = r0;
+    uint32_t rr = r0;
     while (rr < r1) {
-        const int64_t seg = rr / p.rows_pg;
-        const int32_t lr_a = (int32_t)(rr - seg * p.rows_pg);
-        const int32_t rg = (int32_t)(seg % p.n_rg);
-        const int32_t kvh = (int32_t)((seg / p.n_rg) % p.Hkv);
-        const int32_t b = (int32_t)(seg / ((int64_t)p.n_rg * p.Hkv));
-        const int32_t nrows = rows_in_group(p, rg);
-        int64_t seg_stop = (seg + 1) * p.rows_pg;
-        if (seg_stop > r1) seg_stop = r1;
+        const uint32_t seg = rr / rows_pg;
+        const uint32_t lr_a = rr - seg * rows_pg;
+        const uint32_t sl = seg % (hkv * n_rg);  // (kvh, rg) slot inside the sequence
+        const uint32_t b = seg / (hkv * n_rg);
+        const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
+        const uint32_t nrows = (uint32_t)rows_in_group(p, (int32_t)rg);
+        const uint32_t seg_stop = min(seg * rows_pg + rows_pg, r1);
         if (lr_a >= nrows) {  // padding rows of a short group
             rr = seg_stop;
             continue;
         }
-        int32_t lr_end = (int32_t)(seg_stop - seg * p.rows_pg);
-        if (lr_end > nrows) lr_end = nrows;
+        const uint32_t lr_end = min(seg_stop - seg * rows_pg, nrows);
 
         const int32_t su = seg_units(p, lens_s[b]);
-        const int64_t sb = pre_s[b] + ((int64_t)kvh * p.n_rg + rg) * su;
-        int64_t c_first = 0;
-        int32_t n_pieces = 0;
+        const int64_t sb = pre_s[b] + (int64_t)sl * su;
+        int32_t c_first = 0, n_pieces = 0;
         if (su > 0 && barrier_ok) {
-            c_first = cta_of_unit(sb, lo_s, grid);
-            n_pieces = cta_of_unit(sb + su - 1, lo_s, grid) - (int32_t)c_first + 1;
+            c_first = cta_of_unit(sb, lo_s, (int32_t)grid);
+            n_pieces = cta_of_unit(sb + su - 1, lo_s, (int32_t)grid) - c_first + 1;
         }
         const uint32_t per_row = (uint32_t)(n_pieces > 0 ? n_pieces : 1) * REC_BYTES;
-        int32_t nr = (int32_t)(buf_bytes / per_row);
-        if (nr > lr_end - lr_a) nr = lr_end - lr_a;
+        uint32_t nr = min(buf_bytes / per_row, lr_end - lr_a);
         if (nr < 1) nr = 1;  // a single row always fits: pieces <= grid
 
         // stage the records of rows [lr_a, lr_a + nr) of every piece
+        if (warp == 0 && n_pieces > 0) {
+            uint32_t mine = 0;
+            for (int k = lane; k < n_pieces; k += 32) mine += lo_s[c_first + k] != lo_s[c_first + k + 1];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            tc::fence_proxy_async_all();  // partials were written through the generic proxy
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar, mine * nr * REC_BYTES);
+            for (int k = lane; k < n_pieces; k += 32) {
+                const int32_t c = c_first + k;
+                if (lo_s[c] == lo_s[c + 1]) continue;
+                const float *src = p.ws_rec + ((size_t)(seg + c) * rows_pg + lr_a) * REC;
+                tc::bulk_load(tc::smem_u32(buf + (uint32_t)k * nr * REC_BYTES), src, nr * REC_BYTES, bar);
+            }
+        }
         if (threadIdx.x == 0) {
             int ok = 1;
             if (n_pieces > 0) {
-                uint32_t bytes = 0;
-                for (int k = 0; k < n_pieces; ++k)
-                    if (has_units(c_first + k)) bytes += nr * REC_BYTES;
-                tc::fence_proxy_async_all();
-                tc::mbar_arrive_expect_tx(bar, bytes);
-                for (int k = 0; k < n_pieces; ++k) {
-                    const int64_t c = c_first + k;
-                    if (!has_units(c)) continue;
-                    const float *src = p.ws_rec + (slot_of(seg, c) * p.rows_pg + lr_a) * REC;
-                    tc::bulk_load(tc::smem_u32(buf + (uint32_t)k * nr * REC_BYTES), src, nr * REC_BYTES, bar);
-                }
                 const uint64_t t0 = cycles_now();
                 while (!tc::mbar_try_wait(bar, phase)) {
                     if (cycles_now() - t0 > kWaitLimitCycles) {
@@ -335,53 +334,59 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
         if (n_pieces > 0) phase ^= 1;
         const bool staged = ok_s != 0;
 
-        for (int i = warp; i < nr; i += nwarps) {
-            const int32_t lr = lr_a + i;
-            const int32_t r = rg * p.rows_pg + lr;  // packed row
-            const int32_t t = r / p.G, hq = kvh * p.G + (r - t * p.G);
+        for (uint32_t i = warp; i < nr; i += nwarps) {
+            const uint32_t r = rg * rows_pg + lr_a + i;  // packed row
+            const uint32_t t = r / (uint32_t)p.G, hq = kvh * p.G + (r - t * p.G);
             const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
-            // global max over pieces
-            float M = -INFINITY;
-            for (int k0 = 0; k0 < n_pieces; k0 += 32) {
-                const int k = k0 + lane;
-                float m = -INFINITY;
-                if (k < n_pieces && has_units(c_first + k))
-                    m = reinterpret_cast<const float *>(buf + ((uint32_t)k * nr + i) * REC_BYTES)[D];
-                M = fmaxf(M, m);
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float den = 0.f, acc[CPL];
+            const uint8_t *row0 = buf + i * REC_BYTES;
+            const uint32_t pstride = nr * REC_BYTES;  // bytes between pieces
+            float M = -INFINITY, den = 0.f, acc[CPL];
 #pragma unroll
             for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
-            if (M > -INFINITY) {
-                for (int k0 = 0; k0 < n_pieces; k0 += 32) {
-                    const int k = k0 + lane;
-                    float w = 0.f;
-                    if (k < n_pieces && has_units(c_first + k)) {
-                        const float *rec = reinterpret_cast<const float *>(buf + ((uint32_t)k * nr + i) * REC_BYTES);
-                        if (rec[D] > -INFINITY) {
-                            w = exp2f(rec[D] - M);
-                            den += w * rec[D + 1];
-                        }
-                    }
-                    const int nk = n_pieces - k0 < 32 ? n_pieces - k0 : 32;
-                    for (int kk = 0; kk < nk; ++kk) {
-                        const float wk = __shfl_sync(0xffffffffu, w, kk);
-                        if (wk == 0.f) continue;
-                        const float *o = reinterpret_cast<const float *>(
-                                             buf + ((uint32_t)(k0 + kk) * nr + i) * REC_BYTES) + lane * CPL;
+            for (int k0 = 0; k0 < n_pieces; k0 += 32) {
+                // lane k: running max and denominator of piece k0 + k
+                const int k = k0 + lane;
+                float m = -INFINITY, l = 0.f;
+                if (k < n_pieces && lo_s[c_first + k] != lo_s[c_first + k + 1]) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(row0 + (uint32_t)k * pstride + D * 4);
+                    m = ml.x;
+                    l = ml.y;
+                }
+                float Mk = m;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) Mk = fmaxf(Mk, __shfl_xor_sync(0xffffffffu, Mk, o));
+                const float Mn = fmaxf(M, Mk);
+                if (Mn == -INFINITY) continue;
+                // rescale what earlier groups of 32 pieces accumulated
+                const float a = exp2f(M - Mn);
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) acc[c] *= a;
+                den *= a;
+                M = Mn;
+                const float w = m > -INFINITY ? exp2f(m - M) : 0.f;
+                float dl = w * l;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+                den += dl;
+                const int nk = min(32, n_pieces - k0);
+#pragma unroll 4
+                for (int kk = 0; kk < nk; ++kk) {
+                    const float wk = __shfl_sync(0xffffffffu, w, kk);
+                    if (wk != 0.f) {
+                        const float *o = reinterpret_cast<const float *>(row0 + (uint32_t)(k0 + kk) * pstride) + lane * CPL;
                         if constexpr (CPL == 4) {
                             const float4 v = *reinterpret_cast<const float4 *>(o);
-                            acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
+                            acc[0] = fmaf(wk, v.x, acc[0]);
+                            acc[1] = fmaf(wk, v.y, acc[1]);
+                            acc[2] = fmaf(wk, v.z, acc[2]);
+                            acc[3] = fmaf(wk, v.w, acc[3]);
                         } else {
                             const float2 v = *reinterpret_cast<const float2 *>(o);
-                            acc[0] += wk * v.x; acc[1] += wk * v.y;
+                            acc[0] = fmaf(wk, v.x, acc[0]);
+                            acc[1] = fmaf(wk, v.y, acc[1]);
                         }
                     }
                 }
-#pragma unroll
-                for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
             }
             float lse, inv;
             if (!barrier_ok || !staged) {
@@ -408,7 +413,7 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
             if (lane == 0) p.out_lse[out_row] = lse;
         }
         __syncthreads();  // the buffer is reused by the next chunk
-        rr = seg * p.rows_pg + lr_a + nr;
+        rr = seg * rows_pg + lr_a + nr;
     }
 }
 

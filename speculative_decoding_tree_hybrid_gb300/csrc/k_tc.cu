@@ -177,6 +177,13 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     const uint32_t leader = elect_one();
     // K and V are streamed once: keep them from evicting everything else in L2
     const uint64_t policy = l2_evict_first_policy();
+    // Let the first piece's Q rows arrive before the K/V stream starts: issued
+    // behind megabytes of tile requests they would take several microseconds,
+    // and nothing can start without them.
+    if (u0 < u1) {
+        const int halves = (p.rows_pg + kHalf - 1) / kHalf;
+        for (int h = 0; h < halves && ok; ++h) ok = wait_warp(bar_addr(sh.q_full[h]), 0, abort, p.dev_err);
+    }
     while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
