@@ -64,9 +64,9 @@ int choose_path(const hta_dims *d) {
     const int forced = forced_path();
     const bool tc_ok = d->d == 128 && tc_device_ok() && hta::tc_rows_per_group() > 0;
     if (forced == kPathCC) return kPathCC;
-    if (forced == kPathTC) return tc_ok ? kPathTC : kPathNone;
+    if (forced == kPathTC) return (tc_ok && d->Hq / d->Hkv <= hta::tc_rows_per_group()) ? kPathTC : kPathNone;
     const int R = d->T * (d->Hq / d->Hkv);
-    return (tc_ok && R >= 16) ? kPathTC : kPathCC;
+    return (tc_ok && R >= 16 && d->Hq / d->Hkv <= hta::tc_rows_per_group()) ? kPathTC : kPathCC;
 }
 
 struct Layout {
@@ -80,8 +80,16 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
     const int R = d->T * (d->Hq / d->Hkv);
     const int rpg_max = path == kPathTC ? hta::tc_rows_per_group() : hta::cc_rows_per_group();
     L.tile = path == kPathTC ? hta::tc_tile() : hta::cc_tile();
-    L.n_rg = (R + rpg_max - 1) / rpg_max;
-    L.rows_pg = (R + L.n_rg - 1) / L.n_rg;
+    if (path == kPathTC) {
+        // whole tree nodes per group: the tensor-core path loads a group's Q
+        // rows as one box of tpg nodes x G heads
+        const int G = d->Hq / d->Hkv, tpg_max = rpg_max / G;
+        L.n_rg = (d->T + tpg_max - 1) / tpg_max;
+        L.rows_pg = (d->T + L.n_rg - 1) / L.n_rg * G;
+    } else {
+        L.n_rg = (R + rpg_max - 1) / rpg_max;
+        L.rows_pg = (R + L.n_rg - 1) / L.n_rg;
+    }
     L.n_tree_tiles = tree ? (d->T + L.tile - 1) / L.tile : 0;
     L.n_seg = (int64_t)d->B * d->Hkv * L.n_rg;
     L.slots = L.n_seg + grid;

@@ -16,6 +16,7 @@
 //                 128-byte swizzle) into a shared-memory ring;
 //   warp 1        MMA issuer: S_h = Q_h K(i)^T into tensor memory, then
 //                 O_h += P_h V(i) with P read from tensor memory;
+//   warp 2        TMA loads of each piece's Q rows (both halves at once);
 //   warps 4-7     softmax of half 0, one query row per thread;
 //   warps 8-11    softmax of half 1.
 // Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each; P_h
@@ -52,11 +53,11 @@ constexpr int kMaxRows = 256;       // rows per row group
 constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;   // one K or V tile
 constexpr uint32_t kSubBytes = 128 * 64 * 2;     // one 64-dim swizzled sub-tile of it
-constexpr uint32_t kQHalfBytes = 128 * 128 * 2;  // Q rows of one half
-constexpr uint32_t kQSubBytes = 128 * 64 * 2;    // one 64-dim sub-tile of them
+constexpr uint32_t kQSubBytes = kMaxRows * 64 * 2;  // 64 dims of all rows of a group
+constexpr uint32_t kQHalfBytes = kHalf * 128;       // offset of half h inside a sub-tile
 constexpr int kMaxStages = 5;                    // K/V ring stages (4 when the schedule is large)
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffRing = 2 * kQHalfBytes;
+constexpr uint32_t kOffRing = 2 * kQSubBytes;
 constexpr uint32_t kSharedBytes = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;  // S_0, S_1 take columns 0..255
@@ -68,13 +69,13 @@ __host__ __device__ constexpr uint32_t off_shared(int stages) { return kOffRing 
 __host__ __device__ constexpr uint32_t off_sched(int stages) { return off_shared(stages) + kSharedBytes; }
 
 struct TcMaps {
-    CUtensorMap kc, vc, ks, vs;
+    CUtensorMap kc, vc, ks, vs, q;
 };
 
 struct TcShared {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t s_full[2], p_full[2], o_done[2], o_free[2], q_full[2];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2], q_full, q_empty;
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -177,13 +178,6 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     const uint32_t leader = elect_one();
     // K and V are streamed once: keep them from evicting everything else in L2
     const uint64_t policy = l2_evict_first_policy();
-    // Let the first piece's Q rows arrive before the K/V stream starts: issued
-    // behind megabytes of tile requests they would take several microseconds,
-    // and nothing can start without them.
-    if (u0 < u1) {
-        const int halves = (p.rows_pg + kHalf - 1) / kHalf;
-        for (int h = 0; h < halves && ok; ++h) ok = wait_warp(bar_addr(sh.q_full[h]), 0, abort, p.dev_err);
-    }
     while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
@@ -212,12 +206,36 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     }
 }
 
+// Q rows of each piece's row group, by TMA: one box per 64-dim half covering
+// every (tree node, query head) of the group, 128-byte swizzled, zero past
+// the last tree node. The group's rows are t-aligned (rows_pg = tpg * G), so
+// box row t_local * G + g is packed row r_local. A piece's Q replaces the
+// previous one only after the MMAs of that piece have read it (q_empty).
+__device__ void q_loader(const AttnParams &p, const TcMaps &maps, TcShared &sh, uint32_t sQ,
+                         const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+    volatile int32_t *abort = &sh.abort;
+    const uint32_t leader = elect_one();
+    const int tpg = p.rows_pg / p.G;
+    Cursor c;
+    cursor_init(c, u0, u1);
+    TileInfo t;
+    while (cursor_next(c, p, lens_s, pre_s, t)) {
+        if (!t.first) continue;
+        if (t.q > 0 && !wait_warp(bar_addr(sh.q_empty), (t.q - 1) & 1, abort, p.dev_err)) return;
+        const uint32_t full = bar_addr(sh.q_full);
+        mbar_arrive_expect_tx_if(leader, full, (uint32_t)p.rows_pg * 256u);
+        tma_load_4d(leader, sQ, &maps.q, full, 0, t.kvh * p.G, t.rg * tpg, t.b);
+        tma_load_4d(leader, sQ + kQSubBytes, &maps.q, full, 64, t.kvh * p.G, t.rg * tpg, t.b);
+    }
+}
+
 // 8 MMAs over d = 128: S_h[128 x 128] = Q_h[128 x 128] K^T
 __device__ __forceinline__ void issue_qk(uint32_t leader, uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t o = ((kk >> 2) * kSubBytes + (kk & 3) * 32) >> 4;  // same layout for Q and K
-        mma_ss(leader, d_tmem, q_desc + o, k_desc + o, kIdescQK, kk > 0);
+        const uint32_t qo = ((kk >> 2) * kQSubBytes + (kk & 3) * 32) >> 4;
+        const uint32_t ko = ((kk >> 2) * kSubBytes + (kk & 3) * 32) >> 4;
+        mma_ss(leader, d_tmem, q_desc + qo, k_desc + ko, kIdescQK, kk > 0);
     }
 }
 
@@ -231,24 +249,27 @@ __device__ __forceinline__ void issue_pv(uint32_t leader, uint32_t o_tmem, uint3
 }
 
 // S(h,j): waits for K(j) (on the first half) and, at the start of a piece,
-// for the half's Q rows
+// for the group's Q rows; the last S of a piece releases Q
 template <int kStages>
 __device__ __forceinline__ bool issue_s_tile(const AttnParams &p, TcShared &sh, volatile int32_t *abort,
-                                             uint32_t leader, int h, int halves, uint32_t j, bool first, int32_t q,
+                                             uint32_t leader, int h, int halves, uint32_t j, const TileInfo &t,
                                              uint32_t tmem, uint64_t q_desc0, uint64_t k_desc0) {
     const uint32_t n = 2 * j, st = n % kStages, round = n / kStages;
     if (h == 0 && !wait_warp(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return false;
-    if (first && !wait_warp(bar_addr(sh.q_full[h]), q & 1, abort, p.dev_err)) return false;
+    if (t.first && h == 0 && !wait_warp(bar_addr(sh.q_full), t.q & 1, abort, p.dev_err)) return false;
     tc_fence_after();
     issue_qk(leader, tmem + h * 128, q_desc0 + ((h * kQHalfBytes) >> 4), k_desc0 + ((st * kTileBytes) >> 4));
     mma_commit(leader, bar_addr(sh.s_full[h]));
-    if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[st]));
+    if (h == halves - 1) {
+        mma_commit(leader, bar_addr(sh.empty[st]));
+        if (t.last) mma_commit(leader, bar_addr(sh.q_empty));
+    }
     return true;
 }
 
 // Issue order: S(0,0), S(1,0), then per tile i: PV(0,i), S(0,i+1), PV(1,i),
-// S(1,i+1). The first S of a piece waits for that half's new Q rows, which
-// the softmax loads only after reading out the previous piece's O.
+// S(1,i+1). The first S of a piece waits for the piece's Q rows; the first
+// PV of a piece waits until the softmax has read out the previous piece's O.
 template <int kStages>
 __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
                            int halves, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
@@ -264,8 +285,7 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
     bool has_next = cursor_next(c, p, lens_s, pre_s, nxt);
 
     for (int h = 0; h < halves; ++h)
-        if (!issue_s_tile<kStages>(p, sh, abort, leader, h, halves, 0, cur.first, cur.q, tmem, q_desc0, k_desc0))
-            return;
+        if (!issue_s_tile<kStages>(p, sh, abort, leader, h, halves, 0, cur, tmem, q_desc0, k_desc0)) return;
     for (uint32_t i = 0;; ++i) {
         const uint32_t nv = 2 * i + 1, stv = nv % kStages, rv = nv / kStages;
         if (!wait_warp(bar_addr(sh.full[stv]), rv & 1, abort, p.dev_err)) return;
@@ -278,8 +298,7 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             issue_pv(leader, tmem + kColO + h * 128, tmem + h * 128, v_desc, !cur.first);
             if (h == halves - 1) mma_commit(leader, bar_addr(sh.empty[stv]));
             if (cur.last) mma_commit(leader, bar_addr(sh.o_done[h]));
-            if (has_next && !issue_s_tile<kStages>(p, sh, abort, leader, h, halves, i + 1, nxt.first, nxt.q, tmem,
-                                                   q_desc0, k_desc0))
+            if (has_next && !issue_s_tile<kStages>(p, sh, abort, leader, h, halves, i + 1, nxt, tmem, q_desc0, k_desc0))
                 return;
         }
         if (!has_next) break;
@@ -289,7 +308,7 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
 }
 
 template <int kStages>
-__device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint32_t ring, uint32_t tmem,
+__device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uint32_t tmem,
                            int h, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
     const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
@@ -319,24 +338,6 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
             valid = r_local < nrows;
             const int r = t.rg * p.rows_pg + r_local;
             const int tn = valid ? r / p.G : 0;
-            const int hq = t.kvh * p.G + (r - tn * p.G);
-            // this row of Q_h, 128-byte swizzled, zero for padding rows; all
-            // sixteen loads are in flight before the first store
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q + (((int64_t)t.b * p.T + tn) * p.Hq + hq) * 128);
-            uint4 qv[16];
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) qv[ch] = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const uint32_t dst = sQ + h * kQHalfBytes + (ch >> 3) * kQSubBytes + row * 128 +
-                                     (((ch & 7) ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[ch].x),
-                             "r"(qv[ch].y), "r"(qv[ch].z), "r"(qv[ch].w)
-                             : "memory");
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar_addr(sh.q_full[h]));
             if (p.include_tree) {
 #pragma unroll
                 for (int w = 0; w < HTA_TMAX / 32; ++w)
@@ -499,13 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_addr(sh.p_full[h]), 128);
             mbar_init(bar_addr(sh.o_done[h]), 1);
             mbar_init(bar_addr(sh.o_free[h]), 128);
-            mbar_init(bar_addr(sh.q_full[h]), 128);
         }
+        mbar_init(bar_addr(sh.q_full), 1);
+        mbar_init(bar_addr(sh.q_empty), 1);
         mbar_init(bar_addr(sh.drain), 1);
         sh.abort = 0;
         mbar_fence_init();
     }
     if (warp == 0 && (threadIdx.x & 31) == 0) {
+        tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.kc);
         tma_prefetch_desc(&maps.vc);
         if (p.include_tree) {
@@ -532,11 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             producer<kStages>(p, maps, sh, ring, lens_s, pre_s, u0, u1);
         else if (warp == 1)
             mma_issuer<kStages>(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
+        else if (warp == 2)
+            q_loader(p, maps, sh, sQ, lens_s, pre_s, u0, u1);
         __syncwarp();
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 208;");
         const int h = (warp >> 2) - 1;
-        if (h < halves) softmax_wg<kStages>(p, sh, sQ, ring, tmem, h, lens_s, pre_s, u0, u1);
+        if (h < halves) softmax_wg<kStages>(p, sh, ring, tmem, h, lens_s, pre_s, u0, u1);
         __syncwarp();
         asm volatile("setmaxnreg.dec.sync.aligned.u32 168;");
     }
@@ -601,6 +606,20 @@ bool encode_kv(CUtensorMap *map, const void *base, int64_t rows, int64_t heads) 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q [B][T][Hq][d=128] bf16 as a 4-D map; a box is 64 dims x G heads x tpg
+// tree nodes of one sequence (one row group), 128-byte swizzle, zero past T
+bool encode_q(CUtensorMap *map, const void *base, int B, int T, int Hq, int G, int tpg) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {128, (cuuint64_t)Hq, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {128 * 2, (cuuint64_t)Hq * 128 * 2, (cuuint64_t)T * Hq * 128 * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)tpg, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int kStages>
 cudaError_t launch_stages(const AttnParams &p, const TcMaps &maps, int grid, cudaStream_t stream) {
     const size_t smem = tc_smem_bytes(kStages, p.B, grid);
@@ -645,6 +664,9 @@ cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     TcMaps maps;
     memset(&maps, 0, sizeof maps);
     const int64_t heads = (int64_t)p.B * p.Hkv;
+    // row groups must be whole tree nodes (rows_pg = tpg * G, tpg <= 256)
+    if (p.G < 1 || p.rows_pg % p.G != 0 || p.rows_pg > kMaxRows) return cudaErrorInvalidValue;
+    if (!encode_q(&maps.q, p.q, p.B, p.T, p.Hq, p.G, p.rows_pg / p.G)) return cudaErrorInvalidValue;
     if (!encode_kv(&maps.kc, p.k_cache, p.Lmax, heads) || !encode_kv(&maps.vc, p.v_cache, p.Lmax, heads))
         return cudaErrorInvalidValue;
     if (p.include_tree &&

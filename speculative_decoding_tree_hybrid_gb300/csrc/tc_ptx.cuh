@@ -104,6 +104,18 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+// 4-D tiled TMA load issued by the lane with leader != 0
+__device__ __forceinline__ void tma_load_4d(uint32_t leader, uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%1], [%2, {%4, %5, %6, %7}], [%3];\n\t}" ::"r"(leader),
+        "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 // tma_load_3d with an L2 cache policy (see l2_evict_first_policy)
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t leader, uint32_t dst, const CUtensorMap *map,
                                                  uint32_t bar, int x, int y, int z, uint64_t policy) {
