@@ -393,7 +393,7 @@ def run_gpu(args, world, rank, local, pg):
         return
     peak, peak_kind = measured_peak()
     achieved = bytes_step / (us_call * 1e-6) / 1e9
-    kernel = "k_tc_verify" if path == hta.PATH_TC else "k_cc_attn"
+    kernel = {hta.PATH_TC: "k_tc_verify", hta.PATH_TC2: "k_tc2_verify"}.get(path, "k_cc_attn")
     traffic = recorded_traffic(cfg.name, kernel)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -419,7 +419,7 @@ def run_gpu(args, world, rank, local, pg):
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "kv_sets": n_sets,
                    "l2": f"{n_sets} K/V caches of {bytes_step / 1e6:.1f} MB rotated (> 129 MB L2)",
-                   "graph": graph is not None, "path": "tcgen05" if path == hta.PATH_TC else "cuda-core",
+                   "graph": graph is not None, "path": {hta.PATH_TC: "tcgen05", hta.PATH_TC2: "tcgen05 2-CTA clusters"}.get(path, "cuda-core"),
                    "all_bytes_per_call": all_bytes(base)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -1,6 +1,6 @@
 // C-ABI entry points of libhta: argument checks, workspace layout, kernel-path
 // choice and launches. Every step of the computation runs in the kernels of
-// k_mask.cu, k_cc.cu, k_tc.cu and k_merge.cu; this file only validates and
+// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu and k_merge.cu; this file only validates and
 // dispatches.
 #include <math.h>
 #include <stdlib.h>
@@ -47,26 +47,36 @@ hta_status check_dims(const hta_dims *d) {
     return HTA_OK;
 }
 
-enum Path { kPathNone = 0, kPathCC = 1, kPathTC = 2 };
+enum Path { kPathNone = 0, kPathCC = 1, kPathTC = 2, kPathTC2 = 3 };
 
-// Environment override HTA_FORCE_PATH=cc|tc, read on every call.
+// Environment override HTA_FORCE_PATH=cc|tc|tc2, read on every call.
 int forced_path() {
     const char *s = getenv("HTA_FORCE_PATH");
     if (!s) return kPathNone;
     if (!strcmp(s, "cc")) return kPathCC;
     if (!strcmp(s, "tc")) return kPathTC;
+    if (!strcmp(s, "tc2")) return kPathTC2;
     return kPathNone;
 }
 
 // Tensor cores when the head dimension is 128 and the packed query rows of
-// a KV head (T*G) are enough for a dense 128-row MMA tile to be worth it.
+// a KV head (T*G) are enough for a dense 128-row MMA tile to be worth it;
+// past 128 rows, pairs of SMs that share every K/V tile (one 128-row half
+// each), when 2-CTA clusters fit on the device.
+bool tc2_fits(const hta_dims *d) {
+    const int G = d->Hq / d->Hkv;
+    return G <= 64 && hta::tc2_max_grid(d->B, num_sms_current()) >= 2;
+}
+
 int choose_path(const hta_dims *d) {
     const int forced = forced_path();
+    const int G = d->Hq / d->Hkv, R = d->T * G;
     const bool tc_ok = d->d == 128 && tc_device_ok() && hta::tc_rows_per_group() > 0;
     if (forced == kPathCC) return kPathCC;
-    if (forced == kPathTC) return (tc_ok && d->Hq / d->Hkv <= hta::tc_rows_per_group()) ? kPathTC : kPathNone;
-    const int R = d->T * (d->Hq / d->Hkv);
-    return (tc_ok && R >= 16 && d->Hq / d->Hkv <= hta::tc_rows_per_group()) ? kPathTC : kPathCC;
+    if (forced == kPathTC) return (tc_ok && G <= hta::tc_rows_per_group()) ? kPathTC : kPathNone;
+    if (forced == kPathTC2) return (tc_ok && R > 128 && tc2_fits(d)) ? kPathTC2 : kPathNone;
+    if (tc_ok && R > 128 && tc2_fits(d)) return kPathTC2;
+    return (tc_ok && R >= 16 && G <= hta::tc_rows_per_group()) ? kPathTC : kPathCC;
 }
 
 struct Layout {
@@ -79,8 +89,14 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
     Layout L = {};
     const int R = d->T * (d->Hq / d->Hkv);
     const int rpg_max = path == kPathTC ? hta::tc_rows_per_group() : hta::cc_rows_per_group();
-    L.tile = path == kPathTC ? hta::tc_tile() : hta::cc_tile();
-    if (path == kPathTC) {
+    L.tile = path == kPathTC ? hta::tc_tile() : path == kPathTC2 ? hta::tc2_tile() : hta::cc_tile();
+    if (path == kPathTC2) {
+        // whole tree nodes per group, each half of a group at most one
+        // 128-row MMA tile
+        const int G = d->Hq / d->Hkv, tpg_max = 2 * (hta::tc2_rows_per_sub() / G);
+        L.n_rg = (d->T + tpg_max - 1) / tpg_max;
+        L.rows_pg = (d->T + L.n_rg - 1) / L.n_rg * G;
+    } else if (path == kPathTC) {
         // whole tree nodes per group: the tensor-core path loads a group's Q
         // rows as one box of tpg nodes x G heads
         const int G = d->Hq / d->Hkv, tpg_max = rpg_max / G;
@@ -102,6 +118,7 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
 int max_grid(int path, const hta_dims *d) {
     const int sms = num_sms_current();
     if (sms <= 0) return 0;
+    if (path == kPathTC2) return hta::tc2_max_grid(d->B, sms);
     return path == kPathTC ? hta::tc_max_grid(d->B, sms) : hta::cc_max_grid(d->d, d->B, sms);
 }
 
@@ -143,12 +160,16 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
     if (max_units > (int64_t)0x7fffffff || L0.n_seg * (int64_t)L0.rows_pg > (int64_t)0x7fffffff)
         return HTA_ERR_UNSUPPORTED;
     int grid;
+    if (path == kPathTC2 && direct) return HTA_ERR_UNSUPPORTED;  // tree-only calls take the CUDA-core path
     if (direct)
         grid = (int)(L0.n_seg < (int64_t)gmax ? L0.n_seg : gmax);
+    else if (path == kPathTC2)  // one worker per 2-CTA cluster
+        grid = 2 * (int)(max_units < (int64_t)(gmax / 2) ? (max_units > 0 ? max_units : 1) : gmax / 2);
     else
         grid = (int)(max_units < (int64_t)gmax ? (max_units > 0 ? max_units : 1) : gmax);
     Layout L = make_layout(d, path, grid, use_tree);
     AttnParams p = base_params(d, L);
+    p.workers = path == kPathTC2 ? grid / 2 : grid;
     p.q = (const __nv_bfloat16 *)q;
     p.k_cache = (const __nv_bfloat16 *)kc;
     p.v_cache = (const __nv_bfloat16 *)vc;
@@ -170,7 +191,9 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
         p.slots = L.slots;
     }
     cudaError_t e;
-    if (path == kPathTC) {
+    if (path == kPathTC2) {
+        e = hta::tc2_launch(p, grid, stream);
+    } else if (path == kPathTC) {
         if (direct) return HTA_ERR_UNSUPPORTED;  // tree-only calls take the CUDA-core path
         e = hta::tc_launch(p, grid, stream);
     } else {
@@ -212,9 +235,11 @@ hta_status hta_build_mask(const int32_t *parents, int32_t B, int32_t T, uint32_t
 size_t hta_workspace_bytes(const hta_dims *d) {
     if (check_dims(d) != HTA_OK) return 0;
     size_t best = 0;
-    const int paths[2] = {kPathCC, kPathTC};
-    for (int i = 0; i < 2; ++i) {
-        if (paths[i] == kPathTC && !(d->d == 128 && tc_device_ok() && hta::tc_rows_per_group() > 0)) continue;
+    const int paths[3] = {kPathCC, kPathTC, kPathTC2};
+    const bool tc_ok = d->d == 128 && tc_device_ok() && hta::tc_rows_per_group() > 0;
+    for (int i = 0; i < 3; ++i) {
+        if (paths[i] == kPathTC && !tc_ok) continue;
+        if (paths[i] == kPathTC2 && !(tc_ok && tc2_fits(d))) continue;
         const int g = max_grid(paths[i], d);
         if (g <= 0) continue;
         const Layout L = make_layout(d, paths[i], g, true);

@@ -62,6 +62,9 @@ struct AttnParams {
     unsigned int *bar;  // [0] arrivals, [1] departures
     int64_t slots;
     int32_t *dev_err;
+    // schedule: the unit space is split over `workers` (one CTA, or one
+    // cluster of CTAs that share every tile)
+    int32_t workers;
 };
 
 // ---------------------------------------------------------------- errors
@@ -100,7 +103,7 @@ __device__ __forceinline__ int32_t clamp_len(const AttnParams &p, int32_t L) {
 
 // Builds, in shared memory, the clamped lengths lens_s[b], the exclusive
 // prefix pre_s[b] = sum_{b' < b} Hkv * n_rg * seg_units(b') with pre_s[B] = U,
-// and the CTA boundaries lo_s[c] = floor(c * U / grid) for c = 0..grid.
+// and the worker boundaries lo_s[c] = floor(c * U / workers) for c = 0..workers.
 // Warp 0 scans 32 sequences at a time with shuffles; every thread of the
 // block must call it (it ends with __syncthreads). Bad lengths are reported
 // once, by CTA 0.
@@ -133,17 +136,18 @@ __device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int6
     }
     __syncthreads();
     const int64_t U = pre_s[p.B];
-    for (int c = threadIdx.x; c <= (int)gridDim.x; c += blockDim.x) lo_s[c] = ((int64_t)c * U) / gridDim.x;
+    for (int c = threadIdx.x; c <= p.workers; c += blockDim.x) lo_s[c] = ((int64_t)c * U) / p.workers;
     __syncthreads();
 }
 
-// shared-memory bytes of the schedule arrays for B sequences and `grid` CTAs
-__host__ __device__ constexpr size_t sched_bytes(int B, int grid) {
-    return ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8 + (size_t)(grid + 1) * 8;
+// shared-memory bytes of the schedule arrays for B sequences and `workers` workers
+__host__ __device__ constexpr size_t sched_bytes(int B, int workers) {
+    return ((size_t)(B * 4 + 15) / 16) * 16 + (size_t)(B + 1) * 8 + (size_t)(workers + 1) * 8;
 }
 
-// CTA that owns unit u: the largest c < grid with lo_s[c] <= u (CTAs with an
-// empty range share their lo with the next CTA and are never returned).
+// Worker that owns unit u: the largest c < workers with lo_s[c] <= u
+// (workers with an empty range share their lo with the next one and are
+// never returned).
 __device__ __forceinline__ int32_t cta_of_unit(int64_t u, const int64_t *lo_s, int32_t grid) {
     int32_t lo = 0, hi = grid - 1;
     while (lo < hi) {
@@ -195,16 +199,23 @@ __device__ __forceinline__ int32_t rows_in_group(const AttnParams &p, int32_t rg
 
 // ---------------------------------------------------------------- barrier
 
-// Grid-wide barrier for a cooperative launch (every CTA is resident). The
-// wait is bounded by ~2 s of device time; on expiry the error flag is set and
-// the barrier reports failure instead of hanging. Every call returns the two
-// counters to zero once the last CTA has left.
-__device__ inline bool grid_barrier(const AttnParams &p) {
-    __shared__ int ok_s;
+// Grid-wide barrier for a cooperative launch (every CTA is resident), split
+// in two so that a CTA can do independent work between its arrival and the
+// wait. The wait is bounded by ~2 s of device time; on expiry the error flag
+// is set and the barrier reports failure instead of hanging.
+// grid_barrier_depart returns the two counters to zero once the last CTA has
+// left.
+__device__ inline void grid_barrier_arrive(const AttnParams &p) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
+        __threadfence();  // this CTA's partials are visible before it is counted
         atomicAdd(&p.bar[0], 1u);
+    }
+}
+
+__device__ inline bool grid_barrier_wait(const AttnParams &p) {
+    __shared__ int ok_s;
+    if (threadIdx.x == 0) {
         const uint64_t t0 = cycles_now();
         int ok = 1;
         unsigned int v;
@@ -216,7 +227,7 @@ __device__ inline bool grid_barrier(const AttnParams &p) {
                 flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(32);
         }
         __threadfence();
         ok_s = ok;
@@ -244,176 +255,213 @@ __device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return se
 
 // ---------------------------------------------------------------- merge phase
 
-// Merges every output row handled by this CTA. Rows are the packed rows of
-// all segments, linearised segment-major and split evenly over the grid
-// (the host keeps every row and unit count below 2^31, so 32-bit index math
-// is exact). The CTA walks its slice in chunks of consecutive rows of one
-// segment: the lanes of warp 0 bulk-copy the records of those rows from every
-// piece of the segment into `buf` (one copy per piece, all in flight
-// together), then one warp per row reduces them:
+// Merges every output row handled by this CTA, after a grid-wide barrier
+// that it enters here. Rows are the packed rows of all segments, linearised
+// segment-major and split evenly over the grid (the host keeps every row and
+// unit count below 2^31, so 32-bit index math is exact). The CTA's slice is
+// cut into runs, one per segment it touches; between its arrival at the
+// barrier and the wait, one thread per run locates the run's pieces (the CTAs
+// that covered the segment), so that index math overlaps the barrier. Then,
+// chunk by chunk, the lanes of warp 0 bulk-copy the chunk's records of every
+// piece (contiguous per piece) into shared memory, all copies in flight on
+// one mbarrier (the copy engine keeps far more bytes in flight than per-thread
+// loads), and one warp per row applies
 //   M = max_k m_k, w_k = 2^(m_k - M), O = sum_k w_k O_k / sum_k w_k l_k,
-//   LSE = (M + log2 sum_k w_k l_k) ln 2.
+//   LSE = (M + log2 sum_k w_k l_k) ln 2,
+// the log-sum-exp merge of the method ("LongSpec: Long-Context Lossless
+// Speculative Decoding with Efficient Drafting and Verification", Korean
+// summary section 2.C "aggregation"): lanes over pieces for the weights
+// (kept in the records' pad word), then lanes over columns for O.
+// `buf` is idle shared memory (the run table, then the staged records); the
+// block has more than kMergeRuns threads.
+constexpr int kMergeRuns = 64;
+constexpr uint32_t kMergePlanBytes = 5 * kMergeRuns * 4 + 16;  // run table, copy mbarrier, status
+
 template <int D>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
-                                   const int64_t *lo_s, bool barrier_ok, uint8_t *buf, uint32_t buf_bytes) {
-    constexpr int CPL = D / 32;  // columns per lane
-    constexpr int REC = D + 4;   // floats per record
+                                   const int64_t *lo_s, uint8_t *buf, uint32_t buf_bytes) {
+    constexpr int CPL = D / 32;                 // columns per lane
+    constexpr int REC = D + 4;                  // floats per record: O | m | l | w | pad
     constexpr uint32_t REC_BYTES = REC * 4;
-    __shared__ __align__(8) uint64_t mbar;
-    __shared__ int32_t ok_s;
     const uint32_t grid = gridDim.x;
+    const int32_t workers = p.workers;
     const uint32_t rows_pg = (uint32_t)p.rows_pg, n_rg = (uint32_t)p.n_rg, hkv = (uint32_t)p.Hkv;
-    const uint32_t rows_total = (uint32_t)p.B * hkv * n_rg * rows_pg;
+    const uint32_t segs_per_b = hkv * n_rg;
+    const uint32_t rows_total = (uint32_t)p.B * segs_per_b * rows_pg;
     const uint32_t r0 = (uint32_t)(((uint64_t)blockIdx.x * rows_total) / grid);
     const uint32_t r1 = (uint32_t)(((uint64_t)(blockIdx.x + 1) * rows_total) / grid);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-    const uint32_t bar = tc::smem_u32(&mbar);
+    int32_t *run_seg = reinterpret_cast<int32_t *>(buf);
+    int32_t *run_cf = run_seg + kMergeRuns;  // first piece (CTA index)
+    int32_t *run_np = run_cf + kMergeRuns;   // pieces
+    int32_t *run_lo = run_np + kMergeRuns;   // first local row
+    int32_t *run_nr = run_lo + kMergeRuns;   // rows
+    uint8_t *stage = buf + kMergePlanBytes;
+    const uint32_t stage_bytes = buf_bytes - kMergePlanBytes;
+    const uint32_t stage_u32 = tc::smem_u32(stage);
+    const uint32_t bar = tc::smem_u32(buf + 5 * kMergeRuns * 4);
+    volatile int32_t *staged_s = reinterpret_cast<volatile int32_t *>(buf + 5 * kMergeRuns * 4 + 8);
+    uint32_t phase = 0;
     if (threadIdx.x == 0) {
         tc::mbar_init(bar, 1);
         tc::mbar_fence_init();
     }
-    __syncthreads();
-    uint32_t phase = 0;
 
-    uint32_t rr = r0;
-    while (rr < r1) {
-        const uint32_t seg = rr / rows_pg;
-        const uint32_t lr_a = rr - seg * rows_pg;
-        const uint32_t sl = seg % (hkv * n_rg);  // (kvh, rg) slot inside the sequence
-        const uint32_t b = seg / (hkv * n_rg);
-        const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
-        const uint32_t nrows = (uint32_t)rows_in_group(p, (int32_t)rg);
-        const uint32_t seg_stop = min(seg * rows_pg + rows_pg, r1);
-        if (lr_a >= nrows) {  // padding rows of a short group
-            rr = seg_stop;
-            continue;
-        }
-        const uint32_t lr_end = min(seg_stop - seg * rows_pg, nrows);
-
-        const int32_t su = seg_units(p, lens_s[b]);
-        const int64_t sb = pre_s[b] + (int64_t)sl * su;
-        int32_t c_first = 0, n_pieces = 0;
-        if (su > 0 && barrier_ok) {
-            c_first = cta_of_unit(sb, lo_s, (int32_t)grid);
-            n_pieces = cta_of_unit(sb + su - 1, lo_s, (int32_t)grid) - c_first + 1;
-        }
-        const uint32_t per_row = (uint32_t)(n_pieces > 0 ? n_pieces : 1) * REC_BYTES;
-        uint32_t nr = min(buf_bytes / per_row, lr_end - lr_a);
-        if (nr < 1) nr = 1;  // a single row always fits: pieces <= grid
-
-        // stage the records of rows [lr_a, lr_a + nr) of every piece
-        if (warp == 0 && n_pieces > 0) {
-            uint32_t mine = 0;
-            for (int k = lane; k < n_pieces; k += 32) mine += lo_s[c_first + k] != lo_s[c_first + k + 1];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-            tc::fence_proxy_async_all();  // partials were written through the generic proxy
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar, mine * nr * REC_BYTES);
-            for (int k = lane; k < n_pieces; k += 32) {
-                const int32_t c = c_first + k;
-                if (lo_s[c] == lo_s[c + 1]) continue;
-                const float *src = p.ws_rec + ((size_t)(seg + c) * rows_pg + lr_a) * REC;
-                tc::bulk_load(tc::smem_u32(buf + (uint32_t)k * nr * REC_BYTES), src, nr * REC_BYTES, bar);
+    grid_barrier_arrive(p);
+    bool ok = true, waited = false;
+    const uint32_t seg_lo = r0 / rows_pg, seg_end = r1 > r0 ? (r1 - 1) / rows_pg + 1 : seg_lo;
+    for (uint32_t sb = seg_lo; sb < seg_end || !waited; sb += kMergeRuns) {
+        const uint32_t n_runs = sb < seg_end ? min((uint32_t)kMergeRuns, seg_end - sb) : 0u;
+        if (threadIdx.x < n_runs) {
+            const uint32_t seg = sb + threadIdx.x;
+            const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
+            const uint32_t nrows = (uint32_t)rows_in_group(p, (int32_t)(sl % n_rg));
+            const uint32_t base = seg * rows_pg;
+            const uint32_t lo = (r0 > base ? r0 : base) - base;
+            const uint32_t hi = min(r1 - base, nrows);
+            const int32_t su = seg_units(p, lens_s[b]);
+            int32_t cf = 0, np = 0;
+            if (su > 0 && hi > lo) {
+                const int64_t u0 = pre_s[b] + (int64_t)sl * su;
+                cf = cta_of_unit(u0, lo_s, workers);
+                np = cta_of_unit(u0 + su - 1, lo_s, workers) - cf + 1;
             }
+            run_seg[threadIdx.x] = (int32_t)seg;
+            run_cf[threadIdx.x] = cf;
+            run_np[threadIdx.x] = np;
+            run_lo[threadIdx.x] = (int32_t)lo;
+            run_nr[threadIdx.x] = hi > lo ? (int32_t)(hi - lo) : 0;
         }
-        if (threadIdx.x == 0) {
-            int ok = 1;
-            if (n_pieces > 0) {
-                const uint64_t t0 = cycles_now();
-                while (!tc::mbar_try_wait(bar, phase)) {
-                    if (cycles_now() - t0 > kWaitLimitCycles) {
-                        ok = 0;
-                        flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
-                        break;
+        if (!waited) {
+            ok = grid_barrier_wait(p);  // its closing __syncthreads also publishes the table
+            waited = true;
+        } else {
+            __syncthreads();
+        }
+
+        for (uint32_t j = 0; j < n_runs; ++j) {
+            const uint32_t seg = (uint32_t)run_seg[j];
+            const int32_t cf = run_cf[j], np = run_np[j], nrows_run = run_nr[j];
+            const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
+            const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
+            // rows per chunk: every piece's records of the chunk fit in `stage`
+            const uint32_t per_row = (uint32_t)(np > 0 ? np : 1) * REC_BYTES;
+            const int32_t cap = (int32_t)(stage_bytes / per_row) > 0 ? (int32_t)(stage_bytes / per_row) : 1;
+            for (int32_t c0 = 0; c0 < nrows_run; c0 += cap) {
+                const int32_t nr = min(cap, nrows_run - c0);
+                const uint32_t lr0 = (uint32_t)(run_lo[j] + c0);
+                // piece k's records of rows lr0 .. lr0+nr-1 -> stage + k * nr * REC_BYTES
+                const uint32_t bytes = (uint32_t)nr * REC_BYTES;
+                if (ok && warp == 0 && np > 0) {
+                    uint32_t mine = 0;  // non-empty pieces (an empty CTA range wrote nothing)
+                    for (int32_t k = lane; k < np; k += 32) mine += lo_s[cf + k] != lo_s[cf + k + 1];
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+                    // the records were written through the generic proxy by other CTAs
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    if (lane == 0) tc::mbar_arrive_expect_tx(bar, mine * bytes);
+                    for (int32_t k = lane; k < np; k += 32) {
+                        if (lo_s[cf + k] == lo_s[cf + k + 1]) continue;
+                        const float *src = p.ws_rec + ((size_t)(seg + cf + k) * rows_pg + lr0) * REC;
+                        tc::bulk_load(stage_u32 + (uint32_t)k * bytes, src, bytes, bar);
                     }
                 }
-            }
-            ok_s = ok;
-        }
-        __syncthreads();
-        if (n_pieces > 0) phase ^= 1;
-        const bool staged = ok_s != 0;
-
-        for (uint32_t i = warp; i < nr; i += nwarps) {
-            const uint32_t r = rg * rows_pg + lr_a + i;  // packed row
-            const uint32_t t = r / (uint32_t)p.G, hq = kvh * p.G + (r - t * p.G);
-            const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
-            const uint8_t *row0 = buf + i * REC_BYTES;
-            const uint32_t pstride = nr * REC_BYTES;  // bytes between pieces
-            float M = -INFINITY, den = 0.f, acc[CPL];
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
-            for (int k0 = 0; k0 < n_pieces; k0 += 32) {
-                // lane k: running max and denominator of piece k0 + k
-                const int k = k0 + lane;
-                float m = -INFINITY, l = 0.f;
-                if (k < n_pieces && lo_s[c_first + k] != lo_s[c_first + k + 1]) {
-                    const float2 ml = *reinterpret_cast<const float2 *>(row0 + (uint32_t)k * pstride + D * 4);
-                    m = ml.x;
-                    l = ml.y;
-                }
-                float Mk = m;
-#pragma unroll
-                for (int o = 16; o; o >>= 1) Mk = fmaxf(Mk, __shfl_xor_sync(0xffffffffu, Mk, o));
-                const float Mn = fmaxf(M, Mk);
-                if (Mn == -INFINITY) continue;
-                // rescale what earlier groups of 32 pieces accumulated
-                const float a = exp2f(M - Mn);
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[c] *= a;
-                den *= a;
-                M = Mn;
-                const float w = m > -INFINITY ? exp2f(m - M) : 0.f;
-                float dl = w * l;
-#pragma unroll
-                for (int o = 16; o; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
-                den += dl;
-                const int nk = min(32, n_pieces - k0);
-#pragma unroll 4
-                for (int kk = 0; kk < nk; ++kk) {
-                    const float wk = __shfl_sync(0xffffffffu, w, kk);
-                    if (wk != 0.f) {
-                        const float *o = reinterpret_cast<const float *>(row0 + (uint32_t)(k0 + kk) * pstride) + lane * CPL;
-                        if constexpr (CPL == 4) {
-                            const float4 v = *reinterpret_cast<const float4 *>(o);
-                            acc[0] = fmaf(wk, v.x, acc[0]);
-                            acc[1] = fmaf(wk, v.y, acc[1]);
-                            acc[2] = fmaf(wk, v.z, acc[2]);
-                            acc[3] = fmaf(wk, v.w, acc[3]);
-                        } else {
-                            const float2 v = *reinterpret_cast<const float2 *>(o);
-                            acc[0] = fmaf(wk, v.x, acc[0]);
-                            acc[1] = fmaf(wk, v.y, acc[1]);
+                if (threadIdx.x == 0) {
+                    int32_t st = 1;
+                    if (ok && np > 0) {
+                        const uint64_t t0 = cycles_now();
+                        while (!tc::mbar_try_wait(bar, phase)) {
+                            if (cycles_now() - t0 > kWaitLimitCycles) {
+                                flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
+                                st = 0;
+                                break;
+                            }
                         }
                     }
+                    *staged_s = st;
                 }
-            }
-            float lse, inv;
-            if (!barrier_ok || !staged) {
-                lse = __int_as_float(0x7fc00000);
-                inv = __int_as_float(0x7fc00000);
-            } else if (den > 0.f) {
-                lse = (M + log2f(den)) * kLn2;
-                inv = 1.f / den;
-            } else {
-                lse = -INFINITY;  // no visible key: empty softmax
-                inv = 0.f;
-            }
-            if (p.out_fp32) {
-                float *o = (float *)p.out_o + out_row * D + lane * CPL;
+                if (ok && np > 0) phase ^= 1;
+                __syncthreads();
+                ok = ok && *staged_s != 0;  // a timed-out copy leaves NaN outputs from here on
+                const uint32_t pstride = (uint32_t)nr * REC;  // floats between pieces
+                const float *stf = reinterpret_cast<const float *>(stage);
+                for (int32_t i = warp; i < nr; i += nwarps) {
+                    const uint32_t lr = lr0 + (uint32_t)i;
+                    const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
+                    const uint32_t t = r / (uint32_t)p.G, hq = kvh * p.G + (r - t * p.G);
+                    const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
+                    const float *row0 = stf + (uint32_t)i * REC;
+                    float *row0w = const_cast<float *>(row0);
+                    // weights: lanes over pieces
+                    float M = -INFINITY;
+                    for (int32_t k = lane; k < np; k += 32)
+                        if (lo_s[cf + k] != lo_s[cf + k + 1]) M = fmaxf(M, row0[(uint32_t)k * pstride + D]);
 #pragma unroll
-                for (int k = 0; k < CPL; ++k) o[k] = acc[k] * inv;
-            } else {
-                __nv_bfloat16 *o = (__nv_bfloat16 *)p.out_o + out_row * D + lane * CPL;
+                    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                    float den = 0.f;
+                    for (int32_t k = lane; k < np; k += 32) {
+                        float w = 0.f;
+                        if (lo_s[cf + k] != lo_s[cf + k + 1]) {
+                            w = exp2f(row0[(uint32_t)k * pstride + D] - M);
+                            den = fmaf(w, row0[(uint32_t)k * pstride + D + 1], den);
+                        }
+                        row0w[(uint32_t)k * pstride + D + 2] = w;
+                    }
 #pragma unroll
-                for (int k = 0; k < CPL; k += 2)
-                    *reinterpret_cast<__nv_bfloat162 *>(o + k) =
-                        __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+                    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+                    __syncwarp();
+                    float lse, inv;
+                    if (!ok) {
+                        lse = __int_as_float(0x7fc00000);
+                        inv = __int_as_float(0x7fc00000);
+                    } else if (den > 0.f) {
+                        lse = (M + log2f(den)) * kLn2;
+                        inv = 1.f / den;
+                    } else {
+                        lse = -INFINITY;  // no visible key: empty softmax
+                        inv = 0.f;
+                    }
+                    // O: lanes over columns
+                    float acc[CPL];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+                    if (ok) {
+#pragma unroll 4
+                        for (int32_t k = 0; k < np; ++k) {
+                            const float *rec = row0 + (uint32_t)k * pstride;
+                            const float w = rec[D + 2];
+                            if (w != 0.f) {
+                                if constexpr (CPL == 4) {
+                                    const float4 v = *reinterpret_cast<const float4 *>(rec + lane * 4);
+                                    acc[0] = fmaf(w, v.x, acc[0]);
+                                    acc[1] = fmaf(w, v.y, acc[1]);
+                                    acc[2] = fmaf(w, v.z, acc[2]);
+                                    acc[3] = fmaf(w, v.w, acc[3]);
+                                } else {
+                                    const float2 v = *reinterpret_cast<const float2 *>(rec + lane * 2);
+                                    acc[0] = fmaf(w, v.x, acc[0]);
+                                    acc[1] = fmaf(w, v.y, acc[1]);
+                                }
+                            }
+                        }
+                    }
+                    if (p.out_fp32) {
+                        float *op = (float *)p.out_o + out_row * D + lane * CPL;
+#pragma unroll
+                        for (int c = 0; c < CPL; ++c) op[c] = acc[c] * inv;
+                    } else {
+                        __nv_bfloat16 *op = (__nv_bfloat16 *)p.out_o + out_row * D + lane * CPL;
+#pragma unroll
+                        for (int c = 0; c < CPL; c += 2)
+                            *reinterpret_cast<__nv_bfloat162 *>(op + c) =
+                                __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
+                    }
+                    if (lane == 0) p.out_lse[out_row] = lse;
+                }
+                __syncthreads();  // the stage is refilled by the next chunk
             }
-            if (lane == 0) p.out_lse[out_row] = lse;
         }
-        __syncthreads();  // the buffer is reused by the next chunk
-        rr = seg * rows_pg + lr_a + nr;
+        __syncthreads();  // the run table is rewritten by the next batch
     }
 }
 

@@ -19,6 +19,12 @@ int tc_tile();
 int tc_max_grid(int B, int num_sms);
 cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream);
 
+// paired tcgen05 path, clusters of two CTAs sharing every K/V tile (k_tc2.cu)
+int tc2_tile();
+int tc2_rows_per_sub();
+int tc2_max_grid(int B, int num_sms);
+cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream);
+
 // tree mask (k_mask.cu)
 cudaError_t mask_launch(const int32_t *parents, int B, int T, uint32_t *mask, int32_t *dev_err,
                         cudaStream_t stream);

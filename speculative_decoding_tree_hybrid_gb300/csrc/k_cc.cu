@@ -292,9 +292,9 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
         cc_emit<D>(p, st, pos.seg, pos.b, pos.kvh, pos.rg, slot_of(pos.seg, blockIdx.x), false);
         u = piece_end;
     }
-    const bool ok = grid_barrier(p);
-    __syncthreads();  // the tile buffers become the merge staging area
-    merge_phase<D>(p, lens_s, pre_s, lo_s, ok, smem_raw, (uint32_t)sizeof(CcSmem<D>));
+    __syncthreads();  // the tile buffers stage the merge
+    static_assert(sizeof(CcSmem<D>) >= kMergePlanBytes + 32 * (D + 4) * 4, "merge stage too small");
+    merge_phase<D>(p, lens_s, pre_s, lo_s, smem_raw, (uint32_t)sizeof(CcSmem<D>));
     grid_barrier_depart(p);
 }
 

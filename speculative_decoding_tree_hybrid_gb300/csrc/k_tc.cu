@@ -34,18 +34,16 @@
 // issues each TMA / MMA / commit. Every wait is bounded (~4e9 SM cycles,
 // about 2 s); on expiry the kernel sets HTA_DEVERR_TIMEOUT, waits for its own
 // copies in flight, frees its tensor memory and finishes instead of hanging.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "hta_launch.h"
+#include "tc_host.h"
+#include "tc_pipe.cuh"
 #include "tc_ptx.cuh"
 
 namespace hta {
 namespace {
 
 using namespace tc;
+using namespace tcp;
 
 constexpr int kTile = 128;          // keys per tile
 constexpr int kHalf = 128;          // query rows per MMA
@@ -81,87 +79,6 @@ struct TcShared {
     int32_t abort;
 };
 static_assert(sizeof(TcShared) <= kSharedBytes, "shared control block too large");
-
-__device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_u32(&b); }
-
-// Bounded wait on an mbarrier phase; false on timeout or when another warp
-// has aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t *abort,
-                                         int32_t *dev_err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = cycles_now();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return false;
-        if (cycles_now() - t0 > kWaitLimitCycles) {
-            *abort = 1;
-            flag_error(dev_err, HTA_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int32_t *abort, int32_t *dev_err) {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort, dev_err));
-}
-
-// Walks the CTA's unit range tile by tile, piece by piece.
-struct Cursor {
-    int64_t u, u_end;
-    int32_t q;      // piece counter
-    int32_t left;   // tiles left in the current piece
-    int32_t unit;   // next unit index inside the segment
-    int32_t b, kvh, rg, Lb;
-    int64_t seg;
-};
-
-struct TileInfo {
-    int32_t q, unit, b, kvh, rg, Lb;
-    int64_t seg;
-    bool first, last;
-};
-
-__device__ __forceinline__ void cursor_init(Cursor &c, int64_t u0, int64_t u1) {
-    c.u = u0;
-    c.u_end = u1;
-    c.q = -1;
-    c.left = 0;
-    c.unit = 0;
-    c.b = c.kvh = c.rg = c.Lb = 0;
-    c.seg = 0;
-}
-
-__device__ __forceinline__ bool cursor_next(Cursor &c, const AttnParams &p, const int32_t *lens_s,
-                                            const int64_t *pre_s, TileInfo &t) {
-    t.first = false;
-    if (c.left == 0) {
-        if (c.u >= c.u_end) return false;
-        const UnitPos pos = locate_unit(p, c.u, lens_s, pre_s);
-        const int64_t seg_end = pos.seg_begin + pos.seg_units;
-        const int64_t piece_end = seg_end < c.u_end ? seg_end : c.u_end;
-        c.left = (int32_t)(piece_end - c.u);
-        c.unit = pos.unit;
-        c.b = pos.b;
-        c.kvh = pos.kvh;
-        c.rg = pos.rg;
-        c.seg = pos.seg;
-        c.Lb = lens_s[pos.b];
-        c.q += 1;
-        c.u = piece_end;
-        t.first = true;
-    }
-    t.q = c.q;
-    t.unit = c.unit;
-    t.b = c.b;
-    t.kvh = c.kvh;
-    t.rg = c.rg;
-    t.seg = c.seg;
-    t.Lb = c.Lb;
-    c.unit += 1;
-    c.left -= 1;
-    t.last = c.left == 0;
-    return true;
-}
 
 // ------------------------------------------------------------------ roles
 
@@ -557,9 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    const bool ok = grid_barrier(p);
     // Q and the K/V ring are idle now: they stage the merge
-    merge_phase<128>(p, lens_s, pre_s, lo_s, ok, smem + kOffQ, off_shared(kStages) - kOffQ);
+    merge_phase<128>(p, lens_s, pre_s, lo_s, smem + kOffQ, off_shared(kStages) - kOffQ);
     grid_barrier_depart(p);
 }
 
@@ -577,47 +493,6 @@ int tc_stages(int B, int grid) {
     if (tc_smem_bytes(5, B, grid) + slack <= (size_t)max_smem) return 5;
     if (tc_smem_bytes(4, B, grid) + slack <= (size_t)max_smem) return 4;
     return 0;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// [rows][d=128] bf16 per (b, kv head), boxes of 128 rows x 64 dims, 128-byte swizzle
-bool encode_kv(CUtensorMap *map, const void *base, int64_t rows, int64_t heads) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {128, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)heads};
-    const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)(rows > 0 ? rows : 1) * 128 * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// q [B][T][Hq][d=128] bf16 as a 4-D map; a box is 64 dims x G heads x tpg
-// tree nodes of one sequence (one row group), 128-byte swizzle, zero past T
-bool encode_q(CUtensorMap *map, const void *base, int B, int T, int Hq, int G, int tpg) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[4] = {128, (cuuint64_t)Hq, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {128 * 2, (cuuint64_t)Hq * 128 * 2, (cuuint64_t)T * Hq * 128 * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)tpg, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int kStages>
@@ -666,11 +541,11 @@ cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     const int64_t heads = (int64_t)p.B * p.Hkv;
     // row groups must be whole tree nodes (rows_pg = tpg * G, tpg <= 256)
     if (p.G < 1 || p.rows_pg % p.G != 0 || p.rows_pg > kMaxRows) return cudaErrorInvalidValue;
-    if (!encode_q(&maps.q, p.q, p.B, p.T, p.Hq, p.G, p.rows_pg / p.G)) return cudaErrorInvalidValue;
-    if (!encode_kv(&maps.kc, p.k_cache, p.Lmax, heads) || !encode_kv(&maps.vc, p.v_cache, p.Lmax, heads))
+    if (!tch::encode_q(&maps.q, p.q, p.B, p.T, p.Hq, p.G, p.rows_pg / p.G)) return cudaErrorInvalidValue;
+    if (!tch::encode_kv(&maps.kc, p.k_cache, p.Lmax, heads, kTile) || !tch::encode_kv(&maps.vc, p.v_cache, p.Lmax, heads, kTile))
         return cudaErrorInvalidValue;
     if (p.include_tree &&
-        (!encode_kv(&maps.ks, p.k_spec, p.T, heads) || !encode_kv(&maps.vs, p.v_spec, p.T, heads)))
+        (!tch::encode_kv(&maps.ks, p.k_spec, p.T, heads, kTile) || !tch::encode_kv(&maps.vs, p.v_spec, p.T, heads, kTile)))
         return cudaErrorInvalidValue;
     const int stages = tc_stages(p.B, grid);
     if (stages == 5) return launch_stages<5>(p, maps, grid, stream);

@@ -128,6 +128,21 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t leader, uint32_t dst, 
         : "memory");
 }
 
+// tma_load_3d_hint multicast to the CTAs of `mask` in this cluster: the box
+// lands at the same shared-memory offset in each of them and completes bytes
+// on the mbarrier at the same offset in each
+__device__ __forceinline__ void tma_load_3d_mc_hint(uint32_t leader, uint32_t dst, const CUtensorMap *map,
+                                                    uint32_t bar, int x, int y, int z, uint16_t mask,
+                                                    uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%1], [%2, {%4, %5, %6}], [%3], %7, %8;\n\t}" ::"r"(leader),
+        "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask), "l"(policy)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -198,6 +213,34 @@ __device__ __forceinline__ void mma_commit(uint32_t leader, uint32_t bar) {
         "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(leader),
         "r"(bar)
         : "memory");
+}
+
+// mma_commit arriving on the mbarrier at the same offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_mc(uint32_t leader, uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%1], %2;\n\t}"
+        ::"r"(leader), "r"(bar), "h"(mask)
+        : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory state
+// (barrier initialisation) before the peers use it
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator,

@@ -23,7 +23,7 @@ _lock = threading.Lock()
 _lib = None
 _ws_cache: dict = {}
 
-PATH_CC, PATH_TC = 1, 2
+PATH_CC, PATH_TC, PATH_TC2 = 1, 2, 3
 DEVERR_BAD_TREE, DEVERR_CACHE_LEN, DEVERR_TIMEOUT = 1, 2, 4
 TMAX, BMAX = 256, 1024
 

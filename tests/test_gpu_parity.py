@@ -23,7 +23,7 @@ from speculative_decoding_tree_hybrid_gb300 import hta  # noqa: E402
 
 hbuild.build()
 DEV = torch.device("cuda:0")
-PATHS = ["auto", "cc", "tc"]
+PATHS = ["auto", "cc", "tc", "tc2"]
 
 
 @pytest.fixture
@@ -45,12 +45,14 @@ def run_verify(inp, path_name, mask=None, scale=0.0):
         o, lse = hta.verify(t["q"], t["k_cache"], t["v_cache"], t["cache_lens"], t["k_spec"],
                             t["v_spec"], mask, scale=scale, dev_err=err)
     except hta.HtaError as e:
-        if path_name == "tc" and e.status == -2:
-            pytest.skip("tensor-core path unavailable for this shape")
+        if path_name in ("tc", "tc2") and e.status == -2:
+            pytest.skip("this tensor-core path does not take this shape")
         raise
     torch.cuda.synchronize()
     if path_name == "tc":
         assert hta.last_path() == hta.PATH_TC
+    if path_name == "tc2":
+        assert hta.last_path() == hta.PATH_TC2
     if path_name == "cc":
         assert hta.last_path() == hta.PATH_CC
     assert int(err.item()) == 0
@@ -118,6 +120,8 @@ SMALL = [
     (2, 1, 8, 2, 128, [300, 5], "uniform"),         # single node: plain decode
     (1, 200, 4, 2, 64, [90], "uniform"),            # large tree, several tree tiles
     (2, 33, 10, 2, 128, [128, 256], "uniform"),     # G = 5, T not a multiple of 32
+    (1, 100, 16, 4, 128, [900], "window8_depth8"),  # two row groups of 200 rows (two 100-row halves)
+    (1, 65, 16, 4, 128, [600], "uniform"),          # short last row group, odd nodes per group
 ]
 
 
@@ -125,8 +129,8 @@ SMALL = [
 @pytest.mark.parametrize("case", range(len(SMALL)))
 def test_verify_small_every_element(oracle_mod, path, case):
     B, T, Hq, Hkv, d, lens, tree = SMALL[case]
-    if path == "tc" and d != 128:
-        pytest.skip("tensor-core path needs d = 128")
+    if path in ("tc", "tc2") and d != 128:
+        pytest.skip("tensor-core paths need d = 128")
     inp = wl.random_inputs(B, T, Hq, Hkv, d, lens, seed=100 + case, tree=tree)
     o, lse = run_verify(inp, path)
     o_ref, lse_ref = oracle_full(oracle_mod, inp)
@@ -166,7 +170,7 @@ def test_verify_growing_keys_force_rescale(oracle_mod, path):
     assert_close(o, lse, o_ref, lse_ref, "growing keys")
 
 
-@pytest.mark.parametrize("path", ["cc", "tc"], indirect=True)
+@pytest.mark.parametrize("path", ["cc", "tc", "tc2"], indirect=True)
 def test_verify_is_deterministic(path):
     inp = wl.random_inputs(2, 64, 32, 8, 128, [3000, 1700], seed=9, tree="window8_depth8")
     o1, l1 = run_verify(inp, path)
