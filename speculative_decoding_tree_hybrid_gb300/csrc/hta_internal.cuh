@@ -103,14 +103,17 @@ __device__ __forceinline__ int32_t clamp_len(const AttnParams &p, int32_t L) {
 
 // Builds, in shared memory, the clamped lengths lens_s[b], the exclusive
 // prefix pre_s[b] = sum_{b' < b} Hkv * n_rg * seg_units(b') with pre_s[B] = U,
-// and the worker boundaries lo_s[c] = floor(c * U / workers) for c = 0..workers.
+// and the worker boundaries lo_s[c] = floor(c * U / active) for c = 0..workers
+// (c capped at `active`, the workers that get units; see below).
 // Warp 0 scans 32 sequences at a time with shuffles; every thread of the
 // block must call it (it ends with __syncthreads). Bad lengths are reported
 // once, by CTA 0.
 __device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int64_t *pre_s, int64_t *lo_s) {
+    __shared__ int32_t uniform_s;  // every sequence has the same number of units
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        int64_t run = 0;
+        int64_t run = 0, v0 = 0;
+        bool uniform = true;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int b = b0 + lane;
             int64_t v = 0;
@@ -123,6 +126,8 @@ __device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int6
                 lens_s[b] = L;
                 v = (int64_t)p.Hkv * p.n_rg * seg_units(p, L);
             }
+            if (b0 == 0) v0 = __shfl_sync(0xffffffffu, v, 0);
+            uniform = uniform && !__any_sync(0xffffffffu, b < p.B && v != v0);
             int64_t incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -132,11 +137,26 @@ __device__ inline void build_schedule(const AttnParams &p, int32_t *lens_s, int6
             if (b < p.B) pre_s[b] = run + incl - v;
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) pre_s[p.B] = run;
+        if (lane == 0) {
+            pre_s[p.B] = run;
+            uniform_s = uniform ? 1 : 0;
+        }
     }
     __syncthreads();
     const int64_t U = pre_s[p.B];
-    for (int c = threadIdx.x; c <= p.workers; c += blockDim.x) lo_s[c] = ((int64_t)c * U) / p.workers;
+    // When every segment has the same number of units and the workers are
+    // many more than the segments, use only a multiple of the segment count
+    // (at most 1/16 of the workers left idle): each worker then covers part
+    // of exactly one segment, with no switch of KV head or row group (and no
+    // second record) inside its range.
+    int32_t active = p.workers;
+    const int64_t n_seg = (int64_t)p.B * p.Hkv * p.n_rg;
+    if (uniform_s && n_seg > 0 && U > 0 && n_seg <= p.workers) {
+        const int32_t aligned = (int32_t)((p.workers / n_seg) * n_seg);
+        if ((p.workers - aligned) * 16 <= p.workers) active = aligned;
+    }
+    for (int c = threadIdx.x; c <= p.workers; c += blockDim.x)
+        lo_s[c] = ((int64_t)(c < active ? c : active) * U) / active;
     __syncthreads();
 }
 
@@ -181,13 +201,14 @@ __device__ __forceinline__ UnitPos locate_unit(const AttnParams &p, int64_t u, c
     r.b = seq_of_unit(u, pre_s, p.B);
     // skip sequences with zero units (several b may share pre_s)
     r.seg_units = seg_units(p, lens_s[r.b]);
-    const int64_t off = u - pre_s[r.b];
-    const int64_t sl = off / r.seg_units;
-    r.unit = (int32_t)(off - sl * r.seg_units);
-    r.kvh = (int32_t)(sl / p.n_rg);
-    r.rg = (int32_t)(sl - (int64_t)r.kvh * p.n_rg);
+    // unit counts stay below 2^31 (checked on the host): 32-bit division
+    const uint32_t off = (uint32_t)(u - pre_s[r.b]);
+    const uint32_t sl = off / (uint32_t)r.seg_units;
+    r.unit = (int32_t)(off - sl * (uint32_t)r.seg_units);
+    r.kvh = (int32_t)(sl / (uint32_t)p.n_rg);
+    r.rg = (int32_t)(sl - (uint32_t)r.kvh * (uint32_t)p.n_rg);
     r.seg = ((int64_t)r.b * p.Hkv + r.kvh) * p.n_rg + r.rg;
-    r.seg_begin = pre_s[r.b] + sl * r.seg_units;
+    r.seg_begin = pre_s[r.b] + (int64_t)sl * r.seg_units;
     return r;
 }
 

@@ -18,7 +18,8 @@
 // the MMAs of both CTAs have released it. With one 128-row sub-group per SM,
 // tensor memory holds two S buffers next to O, so S(i+1) is computed while
 // the softmax works on tile i and the softmax runs tile after tile:
-//   warp 0      TMA producer (its half of the fills, multicast to the pair)
+//   warps 0, 3  TMA producers of the K ring and the V ring (this CTA's half of
+//               the copies, multicast to the pair)
 //   warp 1      MMA issuer: S(i) = Q K(i)^T into S[i % 2], O += P(i) V(i)
 //   warp 2      TMA loads of each piece's Q rows (double-buffered)
 //   warps 4-7   softmax, one query row per thread
@@ -96,15 +97,34 @@ __device__ __forceinline__ SubGroup sub_group(const AttnParams &p, uint32_t rank
 
 // ------------------------------------------------------------------ roles
 
+// K tiles and V tiles stream through two rings of the same shared memory:
+// K in stages [0, kKStages) and V in stages [kKStages, kStages). A K tile is
+// released as soon as its S has been computed, a V tile only after its PV,
+// so separate rings keep the K stream two tiles ahead of the MMAs. Stage
+// and phase of tile j in each ring:
+constexpr int kKStages = 2;
+template <int kStages>
+__device__ __forceinline__ uint32_t ring_stage(bool is_v, uint32_t j) {
+    return is_v ? kKStages + j % (kStages - kKStages) : j % kKStages;
+}
+template <int kStages>
+__device__ __forceinline__ uint32_t ring_round(bool is_v, uint32_t j) {
+    return is_v ? j / (kStages - kKStages) : j / kKStages;
+}
+
+// One producer warp per ring. Both CTAs expect the bytes of every tile on
+// their own barrier; CTA 0 issues the K copies and CTA 1 the V copies, each
+// multicast to both CTAs.
 template <int kStages>
 __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh, uint32_t ring, uint32_t rank,
-                         const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+                         bool is_v, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
     const int n_tree = p.include_tree ? p.n_tree_tiles : 0;
+    const int ring_n = is_v ? kStages - kKStages : kKStages;
     Cursor c;
     cursor_init(c, u0, u1);
     TileInfo t;
-    uint32_t n = 0;  // ring fills (K(i) is fill 2i, V(i) fill 2i + 1)
+    uint32_t j = 0;  // tiles filled
     bool ok = true;
     const uint32_t leader = elect_one();
     const uint64_t policy = l2_evict_first_policy();  // K and V are read once
@@ -112,27 +132,26 @@ __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int z = t.b * p.Hkv + t.kvh;
-        for (int kv = 0; kv < 2; ++kv, ++n) {
-            const uint32_t st = n % kStages, round = n / kStages;
-            // free in both CTAs (and the previous round of full[st] is complete here)
-            if (!wait_warp(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err)) {
-                ok = false;
-                break;
-            }
-            const uint32_t full = bar_addr(sh.full[st]);
-            mbar_arrive_expect_tx_if(leader, full, kTileBytes);
-            if ((uint32_t)kv == rank) {  // CTA 0 fills K, CTA 1 fills V, for both
-                const CUtensorMap *map = tree ? (kv ? &maps.vs : &maps.ks) : (kv ? &maps.vc : &maps.kc);
-                tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, kPair, policy);
-                tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, kPair, policy);
-            }
+        const uint32_t st = ring_stage<kStages>(is_v, j), round = ring_round<kStages>(is_v, j);
+        // free in both CTAs (and the previous round of full[st] is complete here)
+        if (!wait_warp(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err)) {
+            ok = false;
+            break;
         }
+        const uint32_t full = bar_addr(sh.full[st]);
+        mbar_arrive_expect_tx_if(leader, full, kTileBytes);
+        if ((uint32_t)is_v == rank) {
+            const CUtensorMap *map = tree ? (is_v ? &maps.vs : &maps.ks) : (is_v ? &maps.vc : &maps.kc);
+            tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, kPair, policy);
+            tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, kPair, policy);
+        }
+        ++j;
     }
     if (!ok) {
         // let the copies already issued land before the CTA moves on
         const uint64_t t0 = cycles_now();
-        for (uint32_t k = n > (uint32_t)kStages ? n - kStages : 0; k < n; ++k) {
-            const uint32_t st = k % kStages, round = k / kStages;
+        for (uint32_t k = j > (uint32_t)ring_n ? j - ring_n : 0; k < j; ++k) {
+            const uint32_t st = ring_stage<kStages>(is_v, k), round = ring_round<kStages>(is_v, k);
             while (!mbar_try_wait(bar_addr(sh.full[st]), round & 1))
                 if (cycles_now() - t0 > kWaitLimitCycles) break;
         }
@@ -186,7 +205,7 @@ template <int kStages>
 __device__ __forceinline__ bool issue_s(const AttnParams &p, Tc2Shared &sh, volatile int32_t *abort,
                                         uint32_t leader, uint32_t j, const TileInfo &t, uint32_t tmem,
                                         uint64_t q_desc0, uint64_t k_desc0) {
-    const uint32_t n = 2 * j, st = n % kStages, round = n / kStages;
+    const uint32_t st = ring_stage<kStages>(false, j), round = ring_round<kStages>(false, j);
     const uint32_t qb = t.q & 1;
     if (!wait_warp(bar_addr(sh.full[st]), round & 1, abort, p.dev_err)) return false;
     if (t.first && !wait_warp(bar_addr(sh.q_full[qb]), (t.q >> 1) & 1, abort, p.dev_err)) return false;
@@ -216,7 +235,7 @@ __device__ void mma_issuer(const AttnParams &p, Tc2Shared &sh, uint32_t sQ, uint
     if (has1 && !issue_s<kStages>(p, sh, abort, leader, 1, n1, tmem, q_desc0, k_desc0)) return;
     for (uint32_t i = 0;; ++i) {
         const uint32_t b = i & 1;
-        const uint32_t nv = 2 * i + 1, stv = nv % kStages, rv = nv / kStages;
+        const uint32_t stv = ring_stage<kStages>(true, i), rv = ring_round<kStages>(true, i);
         if (!wait_warp(bar_addr(sh.p_full[b]), (i >> 1) & 1, abort, p.dev_err)) return;
         if (!wait_warp(bar_addr(sh.full[stv]), rv & 1, abort, p.dev_err)) return;
         // O[q % 2] is free once the record of piece q - 2 has been read out
@@ -270,37 +289,42 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         for (int w = 0; w < HTA_TMAX / 32; ++w)
             dst[w] = (v && w < p.W) ? __ldg(p.mask + ((int64_t)pos.b * p.T + tn) * p.W + w) : 0u;
     };
-    // A piece's record is written one tile late, after the next piece's
-    // first P: by then the last PV of the piece has finished (two O
-    // accumulators alternate between pieces), so the softmax does not wait
-    // for it.
+    // A piece's record is written during the next piece, 32 columns after
+    // each of its first tiles: the last PV of the piece has finished by then
+    // (two O accumulators alternate between pieces), and the stores, which
+    // queue behind the K/V stream, come in small batches instead of one
+    // 64 KB burst that would stall the softmax.
     struct Pending {
         bool on, valid;
-        int32_t r_group;
-        uint32_t gi, ob;  // tile of the piece's last PV, O accumulator
+        int32_t r_group, k;  // next 32-column chunk
+        uint32_t gi, ob;     // tile of the piece's last PV, O accumulator
         int64_t slot;
         float m, l;
-    } pend = {false, false, 0, 0, 0, 0, 0.f, 0.f};
+    } pend = {false, false, 0, 0, 0, 0, 0, 0.f, 0.f};
     bool ok = true;
-    auto write_record = [&]() -> bool {
-        if (!wait_warp(bar_addr(sh.pv_done[pend.gi & 1]), (pend.gi >> 1) & 1, abort, p.dev_err)) return false;
-        tc_fence_after();
+    auto write_record = [&](int chunks) -> bool {
+        if (pend.k == 0) {
+            if (!wait_warp(bar_addr(sh.pv_done[pend.gi & 1]), (pend.gi >> 1) & 1, abort, p.dev_err)) return false;
+            tc_fence_after();
+        }
         const uint32_t tOp = tmem + lane_off + kColO + pend.ob * 128;
         float *rec = p.ws_rec + (pend.slot * p.rows_pg + pend.r_group) * 132;
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
+        for (int n = 0; n < chunks && pend.k < 4; ++n, ++pend.k) {
             uint32_t o[32];
-            tmem_ld32(tOp + 32 * k, o);
+            tmem_ld32(tOp + 32 * pend.k, o);
             if (pend.valid) {
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<uint4 *>(rec + 32 * k + e) = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    *reinterpret_cast<uint4 *>(rec + 32 * pend.k + e) = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
             }
         }
-        if (pend.valid) *reinterpret_cast<float2 *>(rec + 128) = make_float2(pend.m, pend.l);
-        tc_fence_before();
-        mbar_arrive(bar_addr(sh.o_free[pend.ob]));
-        pend.on = false;
+        if (pend.k == 4) {
+            if (pend.valid) *reinterpret_cast<float2 *>(rec + 128) = make_float2(pend.m, pend.l);
+            tc_fence_before();
+            mbar_arrive(bar_addr(sh.o_free[pend.ob]));
+            pend.on = false;
+        }
         return true;
     };
 
@@ -320,13 +344,14 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
 #pragma unroll
                     for (int w = 0; w < HTA_TMAX / 32; ++w) mw[w] = mw_next[w];
                 }
+                // the next piece's words: global loads queue behind the K/V
+                // stream for microseconds, so they are issued a piece ahead
+                if (c.u < c.u_end) load_mask(c.u, mw_next);
             }
             m_run = -INFINITY;
             l_run = 0.f;
             o_valid = false;
         }
-        // the next piece's mask words, loaded while this piece ends
-        if (t.last && p.include_tree && c.u < c.u_end) load_mask(c.u, mw_next);
         const bool tree = t.unit < n_tree;
         const int j0 = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int nvalid = tree ? min(kTile, p.T - j0) : min(kTile, t.Lb - j0);
@@ -337,7 +362,7 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         // a partial last cache tile: clear the V rows past the sequence end in
         // this CTA's copy (they may hold anything, and 0 * NaN would poison O)
         if (!tree && nvalid < kTile) {
-            const uint32_t n = 2 * gi + 1, st = n % kStages, round = n / kStages;
+            const uint32_t st = ring_stage<kStages>(true, gi), round = ring_round<kStages>(true, gi);
             ok = wait_bar(bar_addr(sh.full[st]), round & 1, abort, p.dev_err);
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint32_t vb = ring + st * kTileBytes;
@@ -439,11 +464,14 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         mbar_arrive(bar_addr(sh.p_full[b]));
         o_valid = true;
 
-        if (pend.on && !write_record()) break;  // the previous piece's record
-        if (t.last) pend = {true, valid, r_group, gi, (uint32_t)(t.q & 1), slot_of(t.seg, worker), m_run, l_run};
+        if (pend.on && !write_record(1)) break;  // a part of the previous piece's record
+        if (t.last) {
+            if (pend.on && !write_record(4)) break;  // a piece of fewer than four tiles
+            pend = {true, valid, r_group, 0, gi, (uint32_t)(t.q & 1), slot_of(t.seg, worker), m_run, l_run};
+        }
         ++gi;
     }
-    if (pend.on && ok) write_record();
+    if (pend.on && ok) write_record(4);
 }
 
 template <int kStages>
@@ -498,8 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sh.tmem_base;
     const int64_t u0 = lo_s[worker], u1 = lo_s[worker + 1];
 
-    if (warp == 0)
-        producer<kStages>(p, maps, sh, ring, rank, lens_s, pre_s, u0, u1);
+    if (warp == 0 || warp == 3)
+        producer<kStages>(p, maps, sh, ring, rank, warp == 3, lens_s, pre_s, u0, u1);
     else if (warp == 1)
         mma_issuer<kStages>(p, sh, sQ, ring, tmem, lens_s, pre_s, u0, u1);
     else if (warp == 2)
