@@ -97,8 +97,8 @@ def recorded_traffic(workload: str, kernel: str):
     try:
         with open(TRAFFIC_FILE) as fh:
             rec = json.load(fh)
-        e = rec[workload]
-        if e.get("kernel") == kernel and e.get("source_hash") == kernel_source_hash():
+        e = rec[workload][kernel]
+        if e.get("source_hash") == kernel_source_hash():
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass

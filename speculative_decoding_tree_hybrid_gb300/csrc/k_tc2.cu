@@ -485,6 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t *lo_s = pre_s + p.B + 1;
     const uint32_t sQ = smem_u32(smem + kOffQ), ring = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5;
+    // Every cluster operation below (multicast copies and commits, cluster
+    // barriers) assumes a cluster of exactly two CTAs and one worker per
+    // cluster; a launch in any other shape writes nothing and says so.
+    if (cluster_nctarank() != 2 || gridDim.x != 2u * (uint32_t)p.workers || (gridDim.x & 1u)) {
+        if (threadIdx.x == 0) flag_error(p.dev_err, HTA_DEVERR_LAUNCH);
+        return;
+    }
     const uint32_t rank = cluster_ctarank(), worker = cluster_id_x();
 
     if (threadIdx.x == 0) {

@@ -24,7 +24,7 @@ _lib = None
 _ws_cache: dict = {}
 
 PATH_CC, PATH_TC, PATH_TC2 = 1, 2, 3
-DEVERR_BAD_TREE, DEVERR_CACHE_LEN, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_BAD_TREE, DEVERR_CACHE_LEN, DEVERR_TIMEOUT, DEVERR_LAUNCH = 1, 2, 4, 8
 TMAX, BMAX = 256, 1024
 
 # every exported symbol of include/hta.h

@@ -78,12 +78,11 @@ def test_kv_bytes_of_llama_config():
 
 def test_traffic_record_requires_current_sources(tmp_path, monkeypatch):
     f = tmp_path / "traffic.json"
-    f.write_text(json.dumps({"llama8b": {"kernel": "k", "source_hash": "stale",
-                                         "dram_bytes_per_launch": 1.0}}))
+    f.write_text(json.dumps({"llama8b": {"k": {"source_hash": "stale", "dram_bytes_per_launch": 1.0}}}))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     assert bench.recorded_traffic("llama8b", "k") is None
-    f.write_text(json.dumps({"llama8b": {"kernel": "k", "source_hash": bench.kernel_source_hash(),
-                                         "dram_bytes_per_launch": 5.0}}))
+    f.write_text(json.dumps({"llama8b": {"k": {"source_hash": bench.kernel_source_hash(),
+                                               "dram_bytes_per_launch": 5.0}}}))
     assert bench.recorded_traffic("llama8b", "k") == 5.0
     assert bench.recorded_traffic("llama8b", "other") is None
 
