@@ -286,42 +286,48 @@ __device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return se
 // chunk by chunk, the lanes of warp 0 bulk-copy the chunk's records of every
 // piece (contiguous per piece) into shared memory, all copies in flight on
 // one mbarrier (the copy engine keeps far more bytes in flight than per-thread
-// loads), and one warp per row applies
+// loads), and one thread per (row, column chunk) applies
 //   M = max_k m_k, w_k = 2^(m_k - M), O = sum_k w_k O_k / sum_k w_k l_k,
 //   LSE = (M + log2 sum_k w_k l_k) ln 2,
 // the log-sum-exp merge of the method ("LongSpec: Long-Context Lossless
 // Speculative Decoding with Efficient Drafting and Verification", Korean
-// summary section 2.C "aggregation"): lanes over pieces for the weights
-// (kept in the records' pad word), then lanes over columns for O.
+// summary section 2.C "aggregation").
 // `buf` is idle shared memory (the run table, then the staged records); the
 // block has more than kMergeRuns threads.
 constexpr int kMergeRuns = 64;
-constexpr uint32_t kMergePlanBytes = 5 * kMergeRuns * 4 + 16;  // run table, copy mbarrier, status
+constexpr uint32_t kMergePlanBytes = 6 * kMergeRuns * 4 + 16;  // run table, copy mbarrier, status
 
 template <int D>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
                                    const int64_t *lo_s, uint8_t *buf, uint32_t buf_bytes) {
-    constexpr int CPL = D / 32;                 // columns per lane
+    constexpr int HPL = D / 16;                 // columns per lane of a half-warp
     constexpr int REC = D + 4;                  // floats per record: O | m | l | w | pad
     constexpr uint32_t REC_BYTES = REC * 4;
     const uint32_t grid = gridDim.x;
     const int32_t workers = p.workers;
     const uint32_t rows_pg = (uint32_t)p.rows_pg, n_rg = (uint32_t)p.n_rg, hkv = (uint32_t)p.Hkv;
     const uint32_t segs_per_b = hkv * n_rg;
+    // launch parameters used per row, read once
+    const uint32_t G = (uint32_t)p.G, T = (uint32_t)p.T, Hq = (uint32_t)p.Hq;
+    const bool out_fp32 = p.out_fp32 != 0;
+    void *const out_o = p.out_o;
+    float *const out_lse = p.out_lse;
+    const float *const ws_rec = p.ws_rec;
     const uint32_t rows_total = (uint32_t)p.B * segs_per_b * rows_pg;
     const uint32_t r0 = (uint32_t)(((uint64_t)blockIdx.x * rows_total) / grid);
     const uint32_t r1 = (uint32_t)(((uint64_t)(blockIdx.x + 1) * rows_total) / grid);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *run_seg = reinterpret_cast<int32_t *>(buf);
     int32_t *run_cf = run_seg + kMergeRuns;  // first piece (CTA index)
     int32_t *run_np = run_cf + kMergeRuns;   // pieces
     int32_t *run_lo = run_np + kMergeRuns;   // first local row
     int32_t *run_nr = run_lo + kMergeRuns;   // rows
+    int32_t *run_ne = run_nr + kMergeRuns;   // pieces with a record (an empty worker range writes none)
     uint8_t *stage = buf + kMergePlanBytes;
     const uint32_t stage_bytes = buf_bytes - kMergePlanBytes;
     const uint32_t stage_u32 = tc::smem_u32(stage);
-    const uint32_t bar = tc::smem_u32(buf + 5 * kMergeRuns * 4);
-    volatile int32_t *staged_s = reinterpret_cast<volatile int32_t *>(buf + 5 * kMergeRuns * 4 + 8);
+    const uint32_t bar = tc::smem_u32(buf + 6 * kMergeRuns * 4);
+    volatile int32_t *staged_s = reinterpret_cast<volatile int32_t *>(buf + 6 * kMergeRuns * 4 + 8);
     uint32_t phase = 0;
     if (threadIdx.x == 0) {
         tc::mbar_init(bar, 1);
@@ -352,6 +358,9 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
             run_np[threadIdx.x] = np;
             run_lo[threadIdx.x] = (int32_t)lo;
             run_nr[threadIdx.x] = hi > lo ? (int32_t)(hi - lo) : 0;
+            int32_t ne = 0;
+            for (int32_t k = 0; k < np; ++k) ne += lo_s[cf + k] != lo_s[cf + k + 1];
+            run_ne[threadIdx.x] = ne;
         }
         if (!waited) {
             ok = grid_barrier_wait(p);  // its closing __syncthreads also publishes the table
@@ -362,7 +371,8 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
 
         for (uint32_t j = 0; j < n_runs; ++j) {
             const uint32_t seg = (uint32_t)run_seg[j];
-            const int32_t cf = run_cf[j], np = run_np[j], nrows_run = run_nr[j];
+            const int32_t cf = run_cf[j], np = run_np[j], nrows_run = run_nr[j], ne = run_ne[j];
+            const bool dense = ne == np;  // every piece has a record: no per-piece checks below
             const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
             const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
             // rows per chunk: every piece's records of the chunk fit in `stage`
@@ -374,16 +384,12 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                 // piece k's records of rows lr0 .. lr0+nr-1 -> stage + k * nr * REC_BYTES
                 const uint32_t bytes = (uint32_t)nr * REC_BYTES;
                 if (ok && warp == 0 && np > 0) {
-                    uint32_t mine = 0;  // non-empty pieces (an empty CTA range wrote nothing)
-                    for (int32_t k = lane; k < np; k += 32) mine += lo_s[cf + k] != lo_s[cf + k + 1];
-#pragma unroll
-                    for (int o = 16; o; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
                     // the records were written through the generic proxy by other CTAs
                     asm volatile("fence.proxy.async.global;" ::: "memory");
-                    if (lane == 0) tc::mbar_arrive_expect_tx(bar, mine * bytes);
+                    if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)ne * bytes);
                     for (int32_t k = lane; k < np; k += 32) {
-                        if (lo_s[cf + k] == lo_s[cf + k + 1]) continue;
-                        const float *src = p.ws_rec + ((size_t)(seg + cf + k) * rows_pg + lr0) * REC;
+                        if (!dense && lo_s[cf + k] == lo_s[cf + k + 1]) continue;
+                        const float *src = ws_rec + ((size_t)(seg + cf + k) * rows_pg + lr0) * REC;
                         tc::bulk_load(stage_u32 + (uint32_t)k * bytes, src, bytes, bar);
                     }
                 }
@@ -405,79 +411,74 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                 __syncthreads();
                 ok = ok && *staged_s != 0;  // a timed-out copy leaves NaN outputs from here on
                 const uint32_t pstride = (uint32_t)nr * REC;  // floats between pieces
-                const float *stf = reinterpret_cast<const float *>(stage);
-                for (int32_t i = warp; i < nr; i += nwarps) {
+                // one thread per (row, 8-column chunk, or 4 for d = 64): each
+                // computes the piece weights of its row itself (broadcast
+                // shared-memory reads) and its own output columns, so every
+                // load of the chunk is independent of the others
+                constexpr int NCH = D / HPL;  // column chunks per row (16)
+                for (int32_t item = threadIdx.x; item < nr * NCH; item += blockDim.x) {
+                    const int32_t i = item / NCH, ch = item - i * NCH;
                     const uint32_t lr = lr0 + (uint32_t)i;
                     const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
-                    const uint32_t t = r / (uint32_t)p.G, hq = kvh * p.G + (r - t * p.G);
-                    const int64_t out_row = ((int64_t)b * p.T + t) * p.Hq + hq;
-                    const float *row0 = stf + (uint32_t)i * REC;
-                    float *row0w = const_cast<float *>(row0);
-                    // weights: lanes over pieces
+                    const uint32_t t = r / G, hq = kvh * G + (r - t * G);
+                    const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
+                    const float *row0 = reinterpret_cast<const float *>(stage) + (uint32_t)i * REC;
                     float M = -INFINITY;
-                    for (int32_t k = lane; k < np; k += 32)
-                        if (lo_s[cf + k] != lo_s[cf + k + 1]) M = fmaxf(M, row0[(uint32_t)k * pstride + D]);
+                    for (int32_t k = 0; k < np; ++k)
+                        if (dense || lo_s[cf + k] != lo_s[cf + k + 1]) M = fmaxf(M, row0[(uint32_t)k * pstride + D]);
+                    float den = 0.f, acc[HPL];
 #pragma unroll
-                    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                    float den = 0.f;
-                    for (int32_t k = lane; k < np; k += 32) {
-                        float w = 0.f;
-                        if (lo_s[cf + k] != lo_s[cf + k + 1]) {
-                            w = exp2f(row0[(uint32_t)k * pstride + D] - M);
-                            den = fmaf(w, row0[(uint32_t)k * pstride + D + 1], den);
+                    for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
+                    if (ok) {
+#pragma unroll 2
+                        for (int32_t k = 0; k < np; ++k) {
+                            if (!dense && lo_s[cf + k] == lo_s[cf + k + 1]) continue;  // no record
+                            const float *rec = row0 + (uint32_t)k * pstride;
+                            const float2 ml = *reinterpret_cast<const float2 *>(rec + D);
+                            const float w = tc::ex2(ml.x - M);
+                            den = fmaf(w, ml.y, den);
+#pragma unroll
+                            for (int c = 0; c < HPL; c += 4) {
+                                const float4 v = *reinterpret_cast<const float4 *>(rec + ch * HPL + c);
+                                acc[c] = fmaf(w, v.x, acc[c]);
+                                acc[c + 1] = fmaf(w, v.y, acc[c + 1]);
+                                acc[c + 2] = fmaf(w, v.z, acc[c + 2]);
+                                acc[c + 3] = fmaf(w, v.w, acc[c + 3]);
+                            }
                         }
-                        row0w[(uint32_t)k * pstride + D + 2] = w;
                     }
-#pragma unroll
-                    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-                    __syncwarp();
                     float lse, inv;
                     if (!ok) {
                         lse = __int_as_float(0x7fc00000);
                         inv = __int_as_float(0x7fc00000);
                     } else if (den > 0.f) {
-                        lse = (M + log2f(den)) * kLn2;
-                        inv = 1.f / den;
+                        float l2;
+                        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(den));
+                        lse = (M + l2) * kLn2;
+                        inv = __frcp_rn(den);
                     } else {
                         lse = -INFINITY;  // no visible key: empty softmax
                         inv = 0.f;
                     }
-                    // O: lanes over columns
-                    float acc[CPL];
+                    if (out_fp32) {
+                        float *op = (float *)out_o + out_row * D + ch * HPL;
 #pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-                    if (ok) {
-#pragma unroll 4
-                        for (int32_t k = 0; k < np; ++k) {
-                            const float *rec = row0 + (uint32_t)k * pstride;
-                            const float w = rec[D + 2];
-                            if (w != 0.f) {
-                                if constexpr (CPL == 4) {
-                                    const float4 v = *reinterpret_cast<const float4 *>(rec + lane * 4);
-                                    acc[0] = fmaf(w, v.x, acc[0]);
-                                    acc[1] = fmaf(w, v.y, acc[1]);
-                                    acc[2] = fmaf(w, v.z, acc[2]);
-                                    acc[3] = fmaf(w, v.w, acc[3]);
-                                } else {
-                                    const float2 v = *reinterpret_cast<const float2 *>(rec + lane * 2);
-                                    acc[0] = fmaf(w, v.x, acc[0]);
-                                    acc[1] = fmaf(w, v.y, acc[1]);
-                                }
-                            }
+                        for (int c = 0; c < HPL; c += 4)
+                            *reinterpret_cast<float4 *>(op + c) =
+                                make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
+                    } else {
+                        __nv_bfloat16 *op = (__nv_bfloat16 *)out_o + out_row * D + ch * HPL;
+#pragma unroll
+                        for (int c = 0; c < HPL; c += 4) {
+                            const __nv_bfloat162 x = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
+                            const __nv_bfloat162 y = __floats2bfloat162_rn(acc[c + 2] * inv, acc[c + 3] * inv);
+                            uint2 u;
+                            u.x = *reinterpret_cast<const uint32_t *>(&x);
+                            u.y = *reinterpret_cast<const uint32_t *>(&y);
+                            *reinterpret_cast<uint2 *>(op + c) = u;
                         }
                     }
-                    if (p.out_fp32) {
-                        float *op = (float *)p.out_o + out_row * D + lane * CPL;
-#pragma unroll
-                        for (int c = 0; c < CPL; ++c) op[c] = acc[c] * inv;
-                    } else {
-                        __nv_bfloat16 *op = (__nv_bfloat16 *)p.out_o + out_row * D + lane * CPL;
-#pragma unroll
-                        for (int c = 0; c < CPL; c += 2)
-                            *reinterpret_cast<__nv_bfloat162 *>(op + c) =
-                                __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
-                    }
-                    if (lane == 0) p.out_lse[out_row] = lse;
+                    if (ch == 0) out_lse[out_row] = lse;
                 }
                 __syncthreads();  // the stage is refilled by the next chunk
             }

@@ -399,7 +399,9 @@ template <int kStages>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_verify(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned (128-byte swizzle atoms), by pointer arithmetic on the
+    // shared array so that accesses through it stay shared-memory accesses
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     TcShared &sh = *reinterpret_cast<TcShared *>(smem + off_shared(kStages));
     int32_t *lens_s = reinterpret_cast<int32_t *>(smem + off_sched(kStages));
     int64_t *pre_s = reinterpret_cast<int64_t *>(smem + off_sched(kStages) + ((p.B * 4 + 15) / 16) * 16);
