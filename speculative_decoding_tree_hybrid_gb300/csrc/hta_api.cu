@@ -80,7 +80,7 @@ int choose_path(const hta_dims *d) {
 }
 
 struct Layout {
-    int n_rg, rows_pg, tile, n_tree_tiles;
+    int n_rg, rows_pg, tile, n_tree_tiles, subs;
     int64_t n_seg, slots;
     size_t off_rec, total;
 };
@@ -108,7 +108,10 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
     }
     L.n_tree_tiles = tree ? (d->T + L.tile - 1) / L.tile : 0;
     L.n_seg = (int64_t)d->B * d->Hkv * L.n_rg;
-    L.slots = L.n_seg + grid;
+    // record slots: (segment + worker) * records per piece, a staircase of
+    // pieces (the paired kernel has grid / 2 workers)
+    L.subs = 1;
+    L.slots = (L.n_seg + (path == kPathTC2 ? grid / 2 : grid)) * L.subs;
     // [barrier counters | partial records (d + 4 floats per row)]
     L.off_rec = kWsAlign;
     L.total = align_up(L.off_rec + (size_t)L.slots * L.rows_pg * (d->d + 4) * sizeof(float), kWsAlign);
@@ -140,6 +143,7 @@ AttnParams base_params(const hta_dims *d, const Layout &L) {
     p.rows_pg = L.rows_pg;
     p.tile = L.tile;
     p.n_tree_tiles = L.n_tree_tiles;
+    p.subs = L.subs > 0 ? L.subs : 1;
     return p;
 }
 

@@ -65,6 +65,9 @@ struct AttnParams {
     // schedule: the unit space is split over `workers` (one CTA, or one
     // cluster of CTAs that share every tile)
     int32_t workers;
+    // partial records per (segment, worker) piece: a kernel may split a piece
+    // over several softmax accumulators, each written as its own record
+    int32_t subs;
 };
 
 // ---------------------------------------------------------------- errors
@@ -272,7 +275,11 @@ __device__ inline void grid_barrier_depart(const AttnParams &p) {
 
 // ---------------------------------------------------------------- partials
 
-__device__ __forceinline__ int64_t slot_of(int64_t seg, int64_t cta) { return seg + cta; }
+// Record slot of sub-accumulator x of piece (segment seg, worker w): the
+// monotone staircase of pieces makes seg + w unique.
+__device__ __forceinline__ int64_t slot_of(const AttnParams &p, int64_t seg, int64_t w, int32_t x = 0) {
+    return (seg + w) * p.subs + x;
+}
 
 // ---------------------------------------------------------------- merge phase
 
@@ -313,6 +320,7 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
     void *const out_o = p.out_o;
     float *const out_lse = p.out_lse;
     const float *const ws_rec = p.ws_rec;
+    const int32_t subs = p.subs;
     const uint32_t rows_total = (uint32_t)p.B * segs_per_b * rows_pg;
     const uint32_t r0 = (uint32_t)(((uint64_t)blockIdx.x * rows_total) / grid);
     const uint32_t r1 = (uint32_t)(((uint64_t)(blockIdx.x + 1) * rows_total) / grid);
@@ -375,22 +383,23 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
             const bool dense = ne == np;  // every piece has a record: no per-piece checks below
             const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
             const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
-            // rows per chunk: every piece's records of the chunk fit in `stage`
-            const uint32_t per_row = (uint32_t)(np > 0 ? np : 1) * REC_BYTES;
+            // rows per chunk: every record of the chunk fits in `stage`
+            const uint32_t per_row = (uint32_t)(np > 0 ? np * subs : 1) * REC_BYTES;
             const int32_t cap = (int32_t)(stage_bytes / per_row) > 0 ? (int32_t)(stage_bytes / per_row) : 1;
             for (int32_t c0 = 0; c0 < nrows_run; c0 += cap) {
                 const int32_t nr = min(cap, nrows_run - c0);
                 const uint32_t lr0 = (uint32_t)(run_lo[j] + c0);
-                // piece k's records of rows lr0 .. lr0+nr-1 -> stage + k * nr * REC_BYTES
+                // record x of piece k, rows lr0 .. lr0+nr-1 -> stage + (k * subs + x) * nr * REC_BYTES
                 const uint32_t bytes = (uint32_t)nr * REC_BYTES;
                 if (ok && warp == 0 && np > 0) {
                     // the records were written through the generic proxy by other CTAs
                     asm volatile("fence.proxy.async.global;" ::: "memory");
-                    if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)ne * bytes);
-                    for (int32_t k = lane; k < np; k += 32) {
+                    if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)(ne * subs) * bytes);
+                    for (int32_t kx = lane; kx < np * subs; kx += 32) {
+                        const int32_t k = kx / subs;
                         if (!dense && lo_s[cf + k] == lo_s[cf + k + 1]) continue;
-                        const float *src = ws_rec + ((size_t)(seg + cf + k) * rows_pg + lr0) * REC;
-                        tc::bulk_load(stage_u32 + (uint32_t)k * bytes, src, bytes, bar);
+                        const float *src = ws_rec + ((size_t)((seg + cf + k) * subs + (kx - k * subs)) * rows_pg + lr0) * REC;
+                        tc::bulk_load(stage_u32 + (uint32_t)kx * bytes, src, bytes, bar);
                     }
                 }
                 if (threadIdx.x == 0) {
@@ -410,7 +419,8 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                 if (ok && np > 0) phase ^= 1;
                 __syncthreads();
                 ok = ok && *staged_s != 0;  // a timed-out copy leaves NaN outputs from here on
-                const uint32_t pstride = (uint32_t)nr * REC;  // floats between pieces
+                const uint32_t pstride = (uint32_t)nr * REC;  // floats between records
+                const int32_t nrec = np * subs;
                 // one thread per (row, 8-column chunk, or 4 for d = 64): each
                 // computes the piece weights of its row itself (broadcast
                 // shared-memory reads) and its own output columns, so every
@@ -424,15 +434,16 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                     const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
                     const float *row0 = reinterpret_cast<const float *>(stage) + (uint32_t)i * REC;
                     float M = -INFINITY;
-                    for (int32_t k = 0; k < np; ++k)
-                        if (dense || lo_s[cf + k] != lo_s[cf + k + 1]) M = fmaxf(M, row0[(uint32_t)k * pstride + D]);
+                    for (int32_t k = 0; k < nrec; ++k)
+                        if (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1])
+                            M = fmaxf(M, row0[(uint32_t)k * pstride + D]);
                     float den = 0.f, acc[HPL];
 #pragma unroll
                     for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
                     if (ok) {
 #pragma unroll 2
-                        for (int32_t k = 0; k < np; ++k) {
-                            if (!dense && lo_s[cf + k] == lo_s[cf + k + 1]) continue;  // no record
+                        for (int32_t k = 0; k < nrec; ++k) {
+                            if (!dense && lo_s[cf + k / subs] == lo_s[cf + k / subs + 1]) continue;  // no record
                             const float *rec = row0 + (uint32_t)k * pstride;
                             const float2 ml = *reinterpret_cast<const float2 *>(rec + D);
                             const float w = tc::ex2(ml.x - M);

@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
         const int64_t piece_end = seg_end < u_end ? seg_end : u_end;
         const int32_t n = (int32_t)(piece_end - u);
         cc_piece<D>(p, sm, pos.b, pos.kvh, pos.rg, lens_s[pos.b], pos.unit, pos.unit + n, st);
-        cc_emit<D>(p, st, pos.seg, pos.b, pos.kvh, pos.rg, slot_of(pos.seg, blockIdx.x), false);
+        cc_emit<D>(p, st, pos.seg, pos.b, pos.kvh, pos.rg, slot_of(p, pos.seg, blockIdx.x), false);
         u = piece_end;
     }
     __syncthreads();  // the tile buffers stage the merge

@@ -376,7 +376,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
             ok = wait_bar(bar_addr(sh.o_done[h]), t.q & 1, abort, p.dev_err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            float *rec = p.ws_rec + (slot_of(t.seg, blockIdx.x) * p.rows_pg + r_local) * 132;
+            float *rec = p.ws_rec + (slot_of(p, t.seg, blockIdx.x) * p.rows_pg + r_local) * 132;
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) {
                 uint32_t o[32];

@@ -467,7 +467,7 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         if (pend.on && !write_record(1)) break;  // a part of the previous piece's record
         if (t.last) {
             if (pend.on && !write_record(4)) break;  // a piece of fewer than four tiles
-            pend = {true, valid, r_group, 0, gi, (uint32_t)(t.q & 1), slot_of(t.seg, worker), m_run, l_run};
+            pend = {true, valid, r_group, 0, gi, (uint32_t)(t.q & 1), slot_of(p, t.seg, worker), m_run, l_run};
         }
         ++gi;
     }
