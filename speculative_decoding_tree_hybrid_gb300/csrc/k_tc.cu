@@ -281,10 +281,8 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
         for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
         if (!tree && nvalid == kTile) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sa[e]));
-                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sb[e]));
-            }
+            for (int e = 0; e < 64; ++e)
+                mx[e & 7] = fmax3(mx[e & 7], __uint_as_float(sa[e]), __uint_as_float(sb[e]));
         } else {
             // mask words of this tile (a tree has at most two tiles of 128
             // keys); rows past the group see every key (their result is
@@ -298,8 +296,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
                 const bool vb = (e + 64) < nvalid && ((w4[2 + (e >> 5)] >> (e & 31)) & 1u);
                 if (!va) sa[e] = 0xff800000u;  // -inf
                 if (!vb) sb[e] = 0xff800000u;
-                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sa[e]));
-                mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sb[e]));
+                mx[e & 7] = fmax3(mx[e & 7], __uint_as_float(sa[e]), __uint_as_float(sb[e]));
             }
         }
         const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -348,9 +345,10 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float p0 = ex2(fmaf(__uint_as_float(sa[2 * e]), c2, neg_m));
-                const float p1 = ex2(fmaf(__uint_as_float(sa[2 * e + 1]), c2, neg_m));
-                ls[e & 3] += p0 + p1;
+                float x0, x1;  // score pairs through the packed fp32 unit
+                fma2(x0, x1, __uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1]), c2, neg_m);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                add2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                 pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st32(tS, pk);
@@ -359,9 +357,10 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float p0 = ex2(fmaf(__uint_as_float(sb[2 * e]), c2, neg_m));
-                const float p1 = ex2(fmaf(__uint_as_float(sb[2 * e + 1]), c2, neg_m));
-                ls[e & 3] += p0 + p1;
+                float x0, x1;  // score pairs through the packed fp32 unit
+                fma2(x0, x1, __uint_as_float(sb[2 * e]), __uint_as_float(sb[2 * e + 1]), c2, neg_m);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                add2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                 pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st32(tS + 32, pk);
