@@ -1,6 +1,6 @@
 // C-ABI entry points of libhta: argument checks, workspace layout, kernel-path
 // choice and launches. Every step of the computation runs in the kernels of
-// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu and k_merge.cu; this file only validates and
+// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu, k_merge.cu and k_accept.cu; this file only validates and
 // dispatches.
 #include <math.h>
 #include <stdlib.h>
@@ -233,6 +233,25 @@ hta_status hta_build_mask(const int32_t *parents, int32_t B, int32_t T, uint32_t
     if (!parents || !mask || B <= 0 || T <= 0) return HTA_ERR_INVALID_ARG;
     if (T > HTA_TMAX || B > HTA_BMAX) return HTA_ERR_UNSUPPORTED;
     if (hta::mask_launch(parents, B, T, mask, dev_err, stream) != cudaSuccess) return HTA_ERR_CUDA;
+    return HTA_OK;
+}
+
+hta_status hta_accept_commit(const hta_dims *d, const int32_t *parents, const int32_t *draft,
+                             const int32_t *target, const hta_bf16 *k_spec, const hta_bf16 *v_spec,
+                             hta_bf16 *k_cache, hta_bf16 *v_cache, int32_t *cache_lens, int32_t *accepted,
+                             int32_t *n_accepted, int32_t *next_token, int32_t *dev_err,
+                             cudaStream_t stream) {
+    if (!d || !parents || !draft || !target || !k_spec || !v_spec || !k_cache || !v_cache || !cache_lens ||
+        !accepted || !n_accepted || !next_token)
+        return HTA_ERR_INVALID_ARG;
+    if (d->B <= 0 || d->T <= 0 || d->Hkv <= 0 || d->d <= 0 || d->Lmax < 0) return HTA_ERR_INVALID_ARG;
+    if (d->d != 64 && d->d != 128) return HTA_ERR_UNSUPPORTED;
+    if (d->T > HTA_TMAX || d->B > HTA_BMAX || d->Lmax > (int64_t)0x7fffffff) return HTA_ERR_UNSUPPORTED;
+    if (!aligned16(k_spec) || !aligned16(v_spec) || !aligned16(k_cache) || !aligned16(v_cache))
+        return HTA_ERR_ALIGN;
+    if (hta::accept_launch(parents, draft, target, d->B, d->T, d->Hkv, d->d, d->Lmax, k_spec, v_spec, k_cache,
+                           v_cache, cache_lens, accepted, n_accepted, next_token, dev_err, stream) != cudaSuccess)
+        return HTA_ERR_CUDA;
     return HTA_OK;
 }
 

@@ -25,6 +25,12 @@ int tc2_rows_per_sub();
 int tc2_max_grid(int B, int num_sms);
 cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream);
 
+// accept walk and KV commit (k_accept.cu)
+cudaError_t accept_launch(const int32_t *parents, const int32_t *draft, const int32_t *target, int B, int T,
+                          int Hkv, int d, int64_t Lmax, const void *k_spec, const void *v_spec, void *k_cache,
+                          void *v_cache, int32_t *cache_lens, int32_t *accepted, int32_t *n_accepted,
+                          int32_t *next_token, int32_t *dev_err, cudaStream_t stream);
+
 // tree mask (k_mask.cu)
 cudaError_t mask_launch(const int32_t *parents, int B, int T, uint32_t *mask, int32_t *dev_err,
                         cudaStream_t stream);

@@ -29,7 +29,8 @@ TMAX, BMAX = 256, 1024
 
 # every exported symbol of include/hta.h
 EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
-           "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_status_string", "hta_last_path")
+           "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_accept_commit", "hta_status_string",
+           "hta_last_path")
 
 
 class HtaError(RuntimeError):
@@ -69,11 +70,12 @@ def load():
         lib.hta_merge.argtypes = [D, P, P, P, P, P, P, P]
         lib.hta_verify.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
         lib.hta_verify_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
+        lib.hta_accept_commit.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_status_string.argtypes = [ctypes.c_int]
         lib.hta_status_string.restype = ctypes.c_char_p
         lib.hta_last_path.restype = I32
         for name in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge", "hta_verify",
-                     "hta_verify_noalloc"):
+                     "hta_verify_noalloc", "hta_accept_commit"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -263,3 +265,42 @@ def merge(o_c, lse_c, o_s, lse_s):
         _raise(load().hta_merge(ctypes.byref(dims), _ptr(o_c), _ptr(lse_c), _ptr(o_s), _ptr(lse_s),
                                 _ptr(o), _ptr(lse), _stream(dev)), "hta_merge")
     return o, lse
+
+
+def accept_commit(parents, draft, target, k_spec, v_spec, k_cache, v_cache, cache_lens,
+                  dev_err: torch.Tensor | None = None, out=None):
+    """Greedy accept walk over each draft tree and append of the accepted
+    nodes' K/V rows to the cache (k_cache, v_cache and cache_lens change in
+    place). Returns (accepted int32 [B][T] padded with -1, n_accepted int32
+    [B], next_token int32 [B])."""
+    _check(parents, "parents", torch.int32, 2)
+    dev = parents.device
+    _check(draft, "draft", torch.int32, 2, dev)
+    _check(target, "target", torch.int32, 2, dev)
+    _check(k_spec, "k_spec", torch.bfloat16, 4, dev)
+    _check(v_spec, "v_spec", torch.bfloat16, 4, dev)
+    _check(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _check(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _check(cache_lens, "cache_lens", torch.int32, 1, dev)
+    B, T = parents.shape
+    _, Hkv, Lmax, d = k_cache.shape
+    if draft.shape != parents.shape or target.shape != parents.shape:
+        raise ValueError("parents, draft and target must share [B][T]")
+    if tuple(k_spec.shape) != (B, Hkv, T, d) or v_spec.shape != k_spec.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("k_spec/v_spec must be [B][Hkv][T][d] and k_cache/v_cache [B][Hkv][Lmax][d]")
+    if tuple(cache_lens.shape) != (B,):
+        raise ValueError("cache_lens must be [B]")
+    dims = HtaDims(B, T, Hkv, Hkv, d, Lmax, 0.0)
+    if out is None:
+        accepted = torch.empty((B, T), dtype=torch.int32, device=dev)
+        n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
+        nxt = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        accepted, n_acc, nxt = out
+    with torch.cuda.device(dev):
+        _raise(load().hta_accept_commit(ctypes.byref(dims), _ptr(parents), _ptr(draft), _ptr(target),
+                                        _ptr(k_spec), _ptr(v_spec), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(cache_lens), _ptr(accepted), _ptr(n_acc), _ptr(nxt),
+                                        _ptr(dev_err) if dev_err is not None else None, _stream(dev)),
+               "hta_accept_commit")
+    return accepted, n_acc, nxt
