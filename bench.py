@@ -492,6 +492,100 @@ def run_e2e(args, hta, sets, dev, pg):
             "ms_per_step": round(t_max / steps * 1e3, 4)}
 
 
+def accept_inputs(B: int, T: int, seed: int):
+    """Trees of the ragged configs' kind (window-8, depth <= 8), draft tokens,
+    and target predictions that always follow a child, so every walk runs to
+    a leaf (the longest paths the trees allow)."""
+    rng = np.random.default_rng(np.random.SeedSequence([77, seed]))
+    parents = np.stack([wl.tree_window8_depth8(T, rng) for _ in range(B)]).astype(np.int32)
+    draft = rng.integers(0, 32000, size=(B, T)).astype(np.int32)
+    target = np.zeros((B, T), np.int32)
+    for b in range(B):
+        for p in range(T):
+            kids = np.nonzero(parents[b] == p)[0]
+            target[b, p] = draft[b, kids[0]] if len(kids) else 0
+    return parents, draft, target
+
+
+def run_accept(args, world, rank, local, pg):
+    """The step after verification: accept walk + K/V append, timed alone on
+    the ragged B = 32 shape (one layer's K/V).
+
+    The calls are captured in a CUDA graph of kGraph calls, and each timed
+    replay is divided by kGraph: the events see device time only. cache_lens
+    grows by the accepted path every call (Lmax leaves room for all of them).
+    """
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_tree_hybrid_gb300 import hta
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CONFIGS["ragged_b32"]
+    B, T, Hkv, d = cfg.B, cfg.T, cfg.Hkv, cfg.d
+    lens0 = wl.cache_lengths(cfg)
+    warmup, steps = max(args.warmup, 3), min(max(args.steps, 1), 200)
+    k_graph = 20
+    calls = k_graph * (warmup + steps + 1) + warmup
+    # a path is at most depth + 1 = 9 nodes long in these trees
+    Lmax = int(lens0.max()) + 9 * calls + T
+    parents, draft, target = accept_inputs(B, T, seed=1)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in (("p", parents), ("d", draft), ("t", target))}
+    # the step only writes cache rows: their contents need no initialisation
+    kc = torch.empty((B, Hkv, Lmax, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.randn((B, Hkv, T, d), device=dev).to(torch.bfloat16)
+    vs = torch.randn((B, Hkv, T, d), device=dev).to(torch.bfloat16)
+    lens = torch.from_numpy(lens0).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = (torch.empty((B, T), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
+           torch.empty(B, dtype=torch.int32, device=dev))
+
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        def call():
+            hta.accept_commit(t["p"], t["d"], t["t"], ks, vs, kc, vc, lens, dev_err=err, out=out)
+
+        for _ in range(warmup):
+            call()
+        stream.synchronize()
+        n_acc = int(out[1].sum().item())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(k_graph):
+                call()
+        for _ in range(warmup):
+            graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(err.item()):
+        raise SystemExit(f"device error flags {int(err.item())}")
+    times = [a.elapsed_time(b) * 1e3 / k_graph for a, b in ev]
+    us = statistics.median(times)
+    moved = n_acc * Hkv * d * 2 * 2 * 2  # the accepted K and V rows, read once and written once
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    gbs = moved / (us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "accept walk + K/V append, us per call", "op": "accept", "value": round(us, 3), "unit": "us",
+        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": world,
+        "us_p10_p90": [round(float(np.percentile(times, 10)), 3), round(float(np.percentile(times, 90)), 3)],
+        "timing": f"device time per call: CUDA graph of {k_graph} calls per timed replay",
+        "config": {"workload": f"ragged_b32 shape: B={B} T={T} Hkv={Hkv} d={d}, window-8 depth<=8 trees, "
+                               f"target always follows the first child", "accepted_nodes": n_acc},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 5), "peak_source": peak_kind, "bytes_per_call": moved,
+                     "note": "about 1.3 MB per call over 32 CTAs: launch and DRAM latency bound"},
+        "gpu_launches": steps * k_graph, "dtype": "bf16", "data": "synthetic"}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,11 +601,15 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--op", choices=["verify", "accept"], default="verify",
+                    help="verify: the hot path (default); accept: the accept walk + K/V append step alone")
     args = ap.parse_args(argv)
     world, rank, local, pg = dist_setup()
     try:
         if args.impl == "reference":
             run_reference(args, world, rank, pg)
+        elif args.op == "accept":
+            run_accept(args, world, rank, local, pg)
         else:
             run_gpu(args, world, rank, local, pg)
     finally:

@@ -13,14 +13,15 @@
 // HTA_DEVERR_CACHE_LEN).
 //
 // One CTA per sequence. Warp 0 walks the tree from shared memory, 32
-// candidate children per ballot; then all threads copy the path's rows, 16
-// bytes per thread and step.
+// candidate children per ballot; then all threads copy the path's rows in
+// 16-byte chunks, eight loads in flight per thread.
 #include "hta_launch.h"
 
 namespace hta {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kBatch = 8;
 
 __global__ void __launch_bounds__(kThreads)
     k_accept_commit(const int32_t *__restrict__ parents, const int32_t *__restrict__ draft,
@@ -74,15 +75,29 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t room = Lmax - L;
     const int nc = (int64_t)n < room ? n : (int)room;
     if (tid == 0 && nc < n) flag_error(dev_err, HTA_DEVERR_CACHE_LEN);
-    // rows of d bf16 = d / 8 chunks of 16 bytes; K rows then V rows
+    // rows of d bf16 = d / 8 chunks of 16 bytes; K rows then V rows. Each
+    // thread loads up to kBatch chunks before storing any, so a CTA keeps
+    // kBatch x 256 loads in flight instead of one round trip per chunk.
     const int cpr = d / 8;
     const int per_kv = Hkv * nc * cpr;
-    for (int x = tid; x < 2 * per_kv; x += kThreads) {
-        const int kv = x >= per_kv, y = x - kv * per_kv;
-        const int h = y / (nc * cpr), r = y - h * nc * cpr, j = r / cpr, ch = r - j * cpr;
-        const int64_t head = (int64_t)b * Hkv + h;
-        const uint4 v = (kv ? v_spec : k_spec)[(head * T + path_s[j]) * cpr + ch];
-        (kv ? v_cache : k_cache)[(head * Lmax + L + j) * cpr + ch] = v;
+    for (int base = tid; base < 2 * per_kv; base += kBatch * kThreads) {
+        uint4 v[kBatch];
+        int64_t dst[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int x = base + u * kThreads;
+            dst[u] = -1;
+            if (x < 2 * per_kv) {
+                const int kv = x >= per_kv, y = x - kv * per_kv;
+                const int h = y / (nc * cpr), r = y - h * nc * cpr, j = r / cpr, ch = r - j * cpr;
+                const int64_t head = (int64_t)b * Hkv + h;
+                v[u] = (kv ? v_spec : k_spec)[(head * T + path_s[j]) * cpr + ch];
+                dst[u] = ((head * Lmax + L + j) * cpr + ch) * 2 + kv;  // chunk index, K/V in bit 0
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (dst[u] >= 0) ((dst[u] & 1) ? v_cache : k_cache)[dst[u] >> 1] = v[u];
     }
     __syncthreads();  // every thread has read cache_lens[b] (via len_s) before it changes
     if (tid == 0) cache_lens[b] = L + nc;
