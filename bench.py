@@ -586,6 +586,91 @@ def run_accept(args, world, rank, local, pg):
         "gpu_launches": steps * k_graph, "dtype": "bf16", "data": "synthetic"}), flush=True)
 
 
+def run_drafter(args, world, rank, local, pg):
+    """The draft model's two attention kinds, timed alone through CUDA-graph
+    replays (device time per call):
+      cross:  prefix-only attention of one draft query per sequence over the
+              target's KV cache (hta_prefix_attn), LLaMA-3.1-8B layer shape at
+              L = 32768, four K/V sets rotated so the cache is read from HBM;
+      window: sliding-window self-attention (hta_window_attn), W = 512 over a
+              ring of 512 slots, one query per sequence, B = 32 sequences past
+              their first 512 positions (the full window is read)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_tree_hybrid_gb300 import hta
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    warmup, steps = max(args.warmup, 3), min(max(args.steps, 1), 200)
+    Hq, Hkv, d = 32, 8, 128
+    stream = torch.cuda.Stream(dev)
+    if args.op == "cross":
+        B, T, L, sets = 1, 1, 32768, 4
+        gen = torch.Generator(device=dev).manual_seed(7)
+        q = torch.randn((B, T, Hq, d), device=dev, generator=gen).to(torch.bfloat16)
+        kvs = [(torch.randn((B, Hkv, L, d), device=dev, generator=gen).to(torch.bfloat16),
+                torch.randn((B, Hkv, L, d), device=dev, generator=gen).to(torch.bfloat16)) for _ in range(sets)]
+        lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+        dims = hta.dims_of(q, kvs[0][0])
+        ws = hta.workspace(dims, dev)
+
+        def calls():
+            for kc, vc in kvs:
+                hta.prefix_attn(q, kc, vc, lens, ws=ws)
+        per_replay = sets
+        moved = B * L * Hkv * d * 2 * 2
+        workload = f"drafter cross-attention: B={B} draft query per sequence, Hq={Hq} Hkv={Hkv} d={d}, L={L}, " \
+                   f"{sets} K/V sets rotated (> L2)"
+    else:
+        B, T, W = 32, 1, 512
+        gen = torch.Generator(device=dev).manual_seed(8)
+        q = torch.randn((B, T, Hq, d), device=dev, generator=gen).to(torch.bfloat16)
+        kr = torch.randn((B, Hkv, W, d), device=dev, generator=gen).to(torch.bfloat16)
+        vr = torch.randn((B, Hkv, W, d), device=dev, generator=gen).to(torch.bfloat16)
+        pos = torch.randint(W, 100000, (B,), dtype=torch.int32, device=dev, generator=gen)
+        out = (torch.empty_like(q), torch.empty((B, T, Hq), dtype=torch.float32, device=dev))
+
+        def calls():
+            for _ in range(4):
+                hta.window_attn(q, kr, vr, pos, W, out=out)
+        per_replay = 4
+        moved = B * W * Hkv * d * 2 * 2
+        workload = f"drafter sliding-window self-attention: B={B}, T={T}, Hq={Hq} Hkv={Hkv} d={d}, " \
+                   f"window {W} over a ring of {W} slots, every window full"
+    with torch.cuda.stream(stream):
+        calls()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            calls()
+        for _ in range(warmup):
+            graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    times = [a.elapsed_time(b) * 1e3 / per_replay for a, b in ev]
+    us = statistics.median(times)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    gbs = moved / (us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": f"drafter {args.op} attention, us per call", "op": args.op, "value": round(us, 3), "unit": "us",
+        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": world,
+        "us_p10_p90": [round(float(np.percentile(times, 10)), 3), round(float(np.percentile(times, 90)), 3)],
+        "timing": f"device time per call: CUDA graph of {per_replay} calls per timed replay",
+        "config": {"workload": workload},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 5), "peak_source": peak_kind, "bytes_per_call": moved},
+        "path": hta.last_path(), "gpu_launches": steps * per_replay, "dtype": "bf16", "data": "synthetic"}),
+        flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -601,8 +686,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--op", choices=["verify", "accept"], default="verify",
-                    help="verify: the hot path (default); accept: the accept walk + K/V append step alone")
+    ap.add_argument("--op", choices=["verify", "accept", "cross", "window"], default="verify",
+                    help="verify: the hot path (default); accept: the accept walk + K/V append step alone; "
+                         "cross / window: the draft model's cross-attention / sliding-window attention")
     args = ap.parse_args(argv)
     world, rank, local, pg = dist_setup()
     try:
@@ -610,6 +696,8 @@ def main(argv=None):
             run_reference(args, world, rank, pg)
         elif args.op == "accept":
             run_accept(args, world, rank, local, pg)
+        elif args.op in ("cross", "window"):
+            run_drafter(args, world, rank, local, pg)
         else:
             run_gpu(args, world, rank, local, pg)
     finally:

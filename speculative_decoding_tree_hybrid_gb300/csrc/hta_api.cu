@@ -1,6 +1,6 @@
 // C-ABI entry points of libhta: argument checks, workspace layout, kernel-path
 // choice and launches. Every step of the computation runs in the kernels of
-// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu, k_merge.cu and k_accept.cu; this file only validates and
+// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu, k_merge.cu, k_accept.cu and k_window.cu; this file only validates and
 // dispatches.
 #include <math.h>
 #include <stdlib.h>
@@ -252,6 +252,31 @@ hta_status hta_accept_commit(const hta_dims *d, const int32_t *parents, const in
     if (hta::accept_launch(parents, draft, target, d->B, d->T, d->Hkv, d->d, d->Lmax, k_spec, v_spec, k_cache,
                            v_cache, cache_lens, accepted, n_accepted, next_token, dev_err, stream) != cudaSuccess)
         return HTA_ERR_CUDA;
+    return HTA_OK;
+}
+
+hta_status hta_window_attn(const hta_dims *d, int32_t window, const hta_bf16 *q, const hta_bf16 *k_ring,
+                           const hta_bf16 *v_ring, const int32_t *pos, hta_bf16 *o, float *lse, int32_t *dev_err,
+                           cudaStream_t stream) {
+    const hta_status st = check_dims(d);
+    if (st != HTA_OK) return st;
+    if (!q || !k_ring || !v_ring || !pos || !o || !lse) return HTA_ERR_INVALID_ARG;
+    if (window < 1 || d->Lmax < 1) return HTA_ERR_INVALID_ARG;  // the ring holds S = Lmax slots
+    // the first query still reads window - 1 positions older than itself
+    if ((int64_t)window + d->T - 1 > d->Lmax) return HTA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_ring) || !aligned16(v_ring) || !aligned16(o)) return HTA_ERR_ALIGN;
+    Layout L = {};
+    L.n_rg = 1;
+    L.rows_pg = d->T * (d->Hq / d->Hkv);
+    AttnParams p = base_params(d, L);
+    p.q = (const __nv_bfloat16 *)q;
+    p.k_cache = (const __nv_bfloat16 *)k_ring;
+    p.v_cache = (const __nv_bfloat16 *)v_ring;
+    p.out_o = o;
+    p.out_lse = lse;
+    p.dev_err = dev_err;
+    if (hta::window_launch(p, pos, window, (int32_t)d->Lmax, stream) != cudaSuccess) return HTA_ERR_CUDA;
+    g_last_path = kPathCC;
     return HTA_OK;
 }
 

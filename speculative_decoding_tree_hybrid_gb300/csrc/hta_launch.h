@@ -31,6 +31,9 @@ cudaError_t accept_launch(const int32_t *parents, const int32_t *draft, const in
                           void *v_cache, int32_t *cache_lens, int32_t *accepted, int32_t *n_accepted,
                           int32_t *next_token, int32_t *dev_err, cudaStream_t stream);
 
+// draft-model sliding-window (W) self-attention over a ring of S slots (k_window.cu)
+cudaError_t window_launch(const AttnParams &p, const int32_t *pos, int32_t W, int32_t S, cudaStream_t stream);
+
 // tree mask (k_mask.cu)
 cudaError_t mask_launch(const int32_t *parents, int B, int T, uint32_t *mask, int32_t *dev_err,
                         cudaStream_t stream);

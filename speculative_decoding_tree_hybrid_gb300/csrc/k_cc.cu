@@ -5,88 +5,39 @@
 // Drafting and Verification", Korean summary section 2.C: the unmasked cached
 // part and the masked speculative part) as tiles of 64 keys, then merges all
 // partial softmaxes with the log-sum-exp rule after a grid barrier.
-//
-// Block: 8 warps; a row group holds up to 32 packed query rows, 4 per warp.
-// Per 64-key tile: K and V are staged in shared memory (K rows padded so
-// 16-byte reads of 8 consecutive rows hit distinct banks), each lane scores
-// keys lane and lane+32 against its warp's 4 rows, the warp keeps an online
-// softmax in base 2 (scores pre-multiplied by scale*log2 e), and each lane
-// accumulates d/32 adjacent output columns.
+// The per-tile work (staging, scores, online softmax, PV) is in cc_tile.cuh.
+#include "cc_tile.cuh"
 #include "hta_internal.cuh"
 #include "hta_launch.h"
 
 namespace hta {
 namespace {
 
-constexpr int kTile = 64;
-constexpr int kWarps = 8;
-constexpr int kRowsPerWarp = 4;
-constexpr int kRowsPerGroup = kWarps * kRowsPerWarp;  // 32
-constexpr int kThreads = kWarps * 32;
-
-template <int D>
-struct CcSmem {
-    static constexpr int KST = D + 8;  // padded bf16 row stride of the K tile
-    float q[kRowsPerGroup][D];         // scaled queries (scale * log2 e)
-    __nv_bfloat16 k[kTile][KST];
-    __nv_bfloat16 v[kTile][D];
-    float pw[kWarps][kTile][kRowsPerWarp];  // probabilities, [key][row] for float4 broadcast
-};
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-template <int D>
-struct RowState {
-    float m[kRowsPerWarp];
-    float l[kRowsPerWarp];
-    float acc[kRowsPerWarp][D / 32];
-};
+using cct::CcSmem;
+using cct::RowState;
+using cct::kRowsPerGroup;
+using cct::kRowsPerWarp;
+using cct::kThreads;
+using cct::kTile;
 
 // Processes units [u_begin, u_end) of one segment with the CTA's 32-row group.
 template <int D>
 __device__ __forceinline__ void cc_piece(const AttnParams &p, CcSmem<D> &sm, int32_t b, int32_t kvh, int32_t rg,
                          int32_t Lb, int32_t u_begin, int32_t u_end, RowState<D> &st) {
-    constexpr int CPL = D / 32;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int nrows = rows_in_group(p, rg);
     const int r_base = rg * p.rows_pg;
 
     // queries of this row group, scaled, zero for padding rows
     __syncthreads();
-    for (int i = tid; i < kRowsPerGroup * (D / 8); i += kThreads) {
-        const int lr = i / (D / 8), c8 = (i % (D / 8)) * 8;
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (lr < nrows) {
-            const int r = r_base + lr, t = r / p.G, hq = kvh * p.G + (r - t * p.G);
-            const uint4 raw = *reinterpret_cast<const uint4 *>(
-                p.q + (((int64_t)b * p.T + t) * p.Hq + hq) * D + c8);
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 x = __bfloat1622float2(h[k]);
-                f[2 * k] = x.x * p.scale_log2;
-                f[2 * k + 1] = x.y * p.scale_log2;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sm.q[lr][c8 + k] = f[k];
-    }
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-        st.m[i] = -INFINITY;
-        st.l[i] = 0.f;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) st.acc[i][k] = 0.f;
-    }
+    cct::load_q<D>(p, sm, b, [&](int lr, int &t, int &hq) {
+        if (lr >= nrows) return false;
+        const int r = r_base + lr;
+        t = r / p.G;
+        hq = kvh * p.G + (r - t * p.G);
+        return true;
+    });
+    cct::reset<D>(st);
 
     const int n_tree = p.include_tree ? p.n_tree_tiles : 0;
     const int64_t kv_off = ((int64_t)b * p.Hkv + kvh);
@@ -110,99 +61,15 @@ __device__ __forceinline__ void cc_piece(const AttnParams &p, CcSmem<D> &sm, int
             *reinterpret_cast<uint4 *>(&sm.v[j][c8]) = vr;
         }
         __syncthreads();
-
-        // scores for keys lane, lane+32 against rows warp*4 .. warp*4+3
-        float s[kRowsPerWarp][2];
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) s[i][0] = s[i][1] = 0.f;
-#pragma unroll 4
-        for (int c8 = 0; c8 < D; c8 += 8) {
-            float kf[2][8];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.k[lane + 32 * h][c8]);
-                const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&raw);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 x = __bfloat1622float2(hb[k]);
-                    kf[h][2 * k] = x.x;
-                    kf[h][2 * k + 1] = x.y;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const float4 qa = *reinterpret_cast<const float4 *>(&sm.q[warp * kRowsPerWarp + i][c8]);
-                const float4 qb = *reinterpret_cast<const float4 *>(&sm.q[warp * kRowsPerWarp + i][c8 + 4]);
-                const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    s[i][0] = fmaf(qv[k], kf[0][k], s[i][0]);
-                    s[i][1] = fmaf(qv[k], kf[1][k], s[i][1]);
-                }
-            }
-        }
-        // visibility
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int jj = lane + 32 * h;
-            if (jj >= nvalid) {
-#pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i) s[i][h] = -INFINITY;
-            } else if (tree) {
-                const int j = j0 + jj;
-#pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i) {
-                    const int lr = warp * kRowsPerWarp + i;
-                    bool vis = false;
-                    if (lr < nrows) {
-                        const int t = (r_base + lr) / p.G;
-                        const uint32_t w = p.mask[((int64_t)b * p.T + t) * p.W + (j >> 5)];
-                        vis = (w >> (j & 31)) & 1u;
-                    }
-                    if (!vis) s[i][h] = -INFINITY;
-                }
-            }
-        }
-        // online softmax (base 2)
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-            const float mx = warp_max(fmaxf(s[i][0], s[i][1]));
-            const float m_new = fmaxf(st.m[i], mx);
-            float p0 = 0.f, p1 = 0.f, alpha = 1.f;
-            if (m_new > -INFINITY) {
-                alpha = exp2f(st.m[i] - m_new);  // 0 when the old max is -inf
-                p0 = exp2f(s[i][0] - m_new);
-                p1 = exp2f(s[i][1] - m_new);
-                st.m[i] = m_new;
-            }
-            st.l[i] = st.l[i] * alpha + warp_sum(p0 + p1);
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) st.acc[i][k] *= alpha;
-            sm.pw[warp][lane][i] = p0;
-            sm.pw[warp][lane + 32][i] = p1;
-        }
-        __syncwarp();
-        // O += P V
-#pragma unroll 4
-        for (int jj = 0; jj < kTile; ++jj) {
-            const float4 pj = *reinterpret_cast<const float4 *>(&sm.pw[warp][jj][0]);
-            float vf[CPL];
-            if constexpr (CPL == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(&sm.v[jj][lane * 4]);
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
-                const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
-                vf[0] = a.x; vf[1] = a.y; vf[2] = c.x; vf[3] = c.y;
-            } else {
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&sm.v[jj][lane * 2]));
-                vf[0] = a.x; vf[1] = a.y;
-            }
-            const float pv[4] = {pj.x, pj.y, pj.z, pj.w};
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i)
-#pragma unroll
-                for (int k = 0; k < CPL; ++k) st.acc[i][k] = fmaf(pv[i], vf[k], st.acc[i][k]);
-        }
-        __syncwarp();
+        // cache keys are all visible; tree keys per the mask row of the query's node
+        cct::tile<D>(sm, st, nvalid, [&](int i, int jj) {
+            if (!tree) return true;
+            const int lr = warp * kRowsPerWarp + i;
+            if (lr >= nrows) return false;
+            const int t = (r_base + lr) / p.G, j = j0 + jj;
+            const uint32_t w = p.mask[((int64_t)b * p.T + t) * p.W + (j >> 5)];
+            return ((w >> (j & 31)) & 1u) != 0;
+        });
     }
 }
 

@@ -29,7 +29,8 @@ TMAX, BMAX = 256, 1024
 
 # every exported symbol of include/hta.h
 EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
-           "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_accept_commit", "hta_status_string",
+           "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn",
+           "hta_status_string",
            "hta_last_path")
 
 
@@ -71,11 +72,12 @@ def load():
         lib.hta_verify.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
         lib.hta_verify_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_accept_commit.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P]
+        lib.hta_window_attn.argtypes = [D, I32, P, P, P, P, P, P, P, P]
         lib.hta_status_string.argtypes = [ctypes.c_int]
         lib.hta_status_string.restype = ctypes.c_char_p
         lib.hta_last_path.restype = I32
         for name in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge", "hta_verify",
-                     "hta_verify_noalloc", "hta_accept_commit"):
+                     "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -304,3 +306,33 @@ def accept_commit(parents, draft, target, k_spec, v_spec, k_cache, v_cache, cach
                                         _ptr(dev_err) if dev_err is not None else None, _stream(dev)),
                "hta_accept_commit")
     return accepted, n_acc, nxt
+
+
+def window_attn(q, k_ring, v_ring, pos, window: int, *, scale: float = 0.0,
+                dev_err: torch.Tensor | None = None, out: tuple | None = None):
+    """Draft-model sliding-window self-attention: window W over a ring of S
+    slots (k_ring/v_ring [B][Hkv][S][d], position j in slot j mod S,
+    W + T - 1 <= S); the T queries are positions pos[b] .. pos[b] + T - 1.
+    Returns (o bf16 [B][T][Hq][d], lse fp32 [B][T][Hq])."""
+    _check(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _check(k_ring, "k_ring", torch.bfloat16, 4, dev)
+    _check(v_ring, "v_ring", torch.bfloat16, 4, dev)
+    _check(pos, "pos", torch.int32, 1, dev)
+    B, T, Hq, d = q.shape
+    _, Hkv, S, d2 = k_ring.shape
+    if k_ring.shape[0] != B or d2 != d or v_ring.shape != k_ring.shape or tuple(pos.shape) != (B,):
+        raise ValueError("k_ring/v_ring must be [B][Hkv][W][d] and pos [B]")
+    dims = HtaDims(B, T, Hq, Hkv, d, S, float(scale))
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
+    else:
+        o, lse = out
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_window_attn(ctypes.byref(dims), int(window), _ptr(q), _ptr(k_ring), _ptr(v_ring), _ptr(pos),
+                                      _ptr(o), _ptr(lse), _ptr(dev_err), _stream(dev)),
+               "hta_window_attn")
+    return o, lse

@@ -239,3 +239,35 @@ def random_inputs(B: int, T: int, Hq: int, Hkv: int, d: int, lens, *, seed: int,
     ks = normal_bf16(rng, (B, Hkv, T, d))
     vs = normal_bf16(rng, (B, Hkv, T, d))
     return Inputs(cfg, q, kc, vc, lens, ks, vs, parents)
+
+
+# --------------------------------------------------------------------------- draft model
+
+@dataclasses.dataclass
+class WindowInputs:
+    q: np.ndarray       # [B][T][Hq][d] bf16 bits
+    k_ring: np.ndarray  # [B][Hkv][S][d] bf16 bits, position j in slot j mod S
+    v_ring: np.ndarray
+    pos: np.ndarray     # [B] int32: position of query 0
+
+    @property
+    def S(self) -> int:
+        return int(self.k_ring.shape[2])
+
+
+def window_inputs(B: int, T: int, Hq: int, Hkv: int, d: int, S: int, pos, *, seed: int) -> WindowInputs:
+    """Queries at positions pos[b] .. pos[b] + T - 1 and a ring of S slots
+    holding positions max(0, pos[b] + T - S) .. pos[b] + T - 1 (N(0,1) values
+    rounded to bf16, like every other input); slots that hold no position yet
+    are NaN, so a read of one shows up."""
+    pos = np.asarray(pos, dtype=np.int32).reshape(B)
+    rng = np.random.default_rng(np.random.SeedSequence([2000, seed]))
+    q = normal_bf16(rng, (B, T, Hq, d))
+    kr = np.full((B, Hkv, S, d), BF16_NAN, dtype=np.uint16)
+    vr = np.full((B, Hkv, S, d), BF16_NAN, dtype=np.uint16)
+    for b in range(B):
+        end = int(pos[b]) + T
+        js = np.arange(max(0, end - S), end)
+        kr[b][:, js % S] = normal_bf16(rng, (Hkv, len(js), d))
+        vr[b][:, js % S] = normal_bf16(rng, (Hkv, len(js), d))
+    return WindowInputs(q, kr, vr, pos)
