@@ -59,10 +59,11 @@ int forced_path() {
     return kPathNone;
 }
 
-// Tensor cores when the head dimension is 128 and the packed query rows of
-// a KV head (T*G) are enough for a dense 128-row MMA tile to be worth it;
-// past 128 rows, pairs of SMs that share every K/V tile (one 128-row half
-// each), when 2-CTA clusters fit on the device.
+// Tensor cores whenever the head dimension is 128: even a decode-shaped call
+// (a few packed rows per KV head) streams the cache faster through the TMA
+// pipeline of the tensor-core kernel (its 128-row tile has room to spare) than
+// through the CUDA-core kernel. Past 128 rows, pairs of SMs that share every
+// K/V tile (one 128-row half each), when 2-CTA clusters fit on the device.
 bool tc2_fits(const hta_dims *d) {
     const int G = d->Hq / d->Hkv;
     return G <= 64 && hta::tc2_max_grid(d->B, num_sms_current()) >= 2;
@@ -76,7 +77,7 @@ int choose_path(const hta_dims *d) {
     if (forced == kPathTC) return (tc_ok && G <= hta::tc_rows_per_group()) ? kPathTC : kPathNone;
     if (forced == kPathTC2) return (tc_ok && R > 128 && tc2_fits(d)) ? kPathTC2 : kPathNone;
     if (tc_ok && R > 128 && tc2_fits(d)) return kPathTC2;
-    return (tc_ok && R >= 16 && G <= hta::tc_rows_per_group()) ? kPathTC : kPathCC;
+    return (tc_ok && G <= hta::tc_rows_per_group()) ? kPathTC : kPathCC;
 }
 
 struct Layout {
