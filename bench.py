@@ -671,6 +671,71 @@ def run_drafter(args, world, rank, local, pg):
         flush=True)
 
 
+def run_lspec(args, world, rank, local, pg):
+    """The LogitSpec draft-tree builder, timed alone through CUDA-graph
+    replays: B = 32 sequences, LLaMA-3 vocabulary (128256 logits), 32K-token
+    histories with copy structure, logits that favour tokens of the context
+    (so the queries hit), k = 60 next-next guesses (the pages' top-60
+    observation), 3-gram queries, trees of 64 nodes, budget 16 for the x_{i+1}
+    branch and 8 - r // 8 (at least 1) for guess r."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_tree_hybrid_gb300 import hta
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    warmup, steps = max(args.warmup, 3), min(max(args.steps, 1), 200)
+    B, V, Lh, k, m, T = 32, 128256, 32768, 60, 3, 64
+    keep = [16] + [max(1, 8 - r // 8) for r in range(1, k + 1)]
+    logits, hist, lens = wl.lspec_inputs(B, V, Lh, [Lh] * B, seed=5, vocab_used=4000, plant_m=m)
+    lg = torch.from_numpy(logits).to(dev)
+    hs = torch.from_numpy(hist).to(dev)
+    ln = torch.from_numpy(lens).to(dev)
+    out = (torch.empty((B, T), dtype=torch.int32, device=dev), torch.empty((B, T), dtype=torch.int32, device=dev),
+           torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    stream = torch.cuda.Stream(dev)
+    per_replay = 4
+    with torch.cuda.stream(stream):
+        def calls():
+            for _ in range(per_replay):
+                hta.logitspec_tree(lg, hs, ln, k, m, keep, T, out=out)
+        calls()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            calls()
+        for _ in range(warmup):
+            graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    times = [a.elapsed_time(b) * 1e3 / per_replay for a, b in ev]
+    us = statistics.median(times)
+    nodes = int(out[2].sum().item())
+    if rank != 0:
+        return
+    moved = B * V * 4 + B * Lh * 4 + 2 * B * T * 4  # logits and history read once, the trees written
+    peak, peak_kind = measured_peak()
+    gbs = moved / (us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "LogitSpec draft-tree build, us per call", "op": "lspec", "value": round(us, 3), "unit": "us",
+        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": world,
+        "us_p10_p90": [round(float(np.percentile(times, 10)), 3), round(float(np.percentile(times, 90)), 3)],
+        "timing": f"device time per call: CUDA graph of {per_replay} calls per timed replay",
+        "config": {"workload": f"B={B} V={V} history {Lh} tokens (copy spans over a 4000-token vocabulary), "
+                               f"k={k} m={m} T={T}", "real_nodes": nodes},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 5), "peak_source": peak_kind, "bytes_per_call": moved,
+                     "note": "the radix select reads the logits five times (four passes and the gather), "
+                             "from L2 after the first"},
+        "gpu_launches": steps * per_replay, "dtype": "int32/fp32", "data": "synthetic"}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -686,9 +751,10 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--op", choices=["verify", "accept", "cross", "window"], default="verify",
+    ap.add_argument("--op", choices=["verify", "accept", "cross", "window", "lspec"], default="verify",
                     help="verify: the hot path (default); accept: the accept walk + K/V append step alone; "
-                         "cross / window: the draft model's cross-attention / sliding-window attention")
+                         "cross / window: the draft model's cross-attention / sliding-window attention; "
+                         "lspec: the LogitSpec draft-tree builder")
     args = ap.parse_args(argv)
     world, rank, local, pg = dist_setup()
     try:
@@ -698,6 +764,8 @@ def main(argv=None):
             run_accept(args, world, rank, local, pg)
         elif args.op in ("cross", "window"):
             run_drafter(args, world, rank, local, pg)
+        elif args.op == "lspec":
+            run_lspec(args, world, rank, local, pg)
         else:
             run_gpu(args, world, rank, local, pg)
     finally:

@@ -1,6 +1,6 @@
 // C-ABI entry points of libhta: argument checks, workspace layout, kernel-path
 // choice and launches. Every step of the computation runs in the kernels of
-// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu, k_merge.cu, k_accept.cu and k_window.cu; this file only validates and
+// k_mask.cu, k_cc.cu, k_tc.cu, k_tc2.cu, k_merge.cu, k_accept.cu, k_window.cu and k_lspec.cu; this file only validates and
 // dispatches.
 #include <math.h>
 #include <stdlib.h>
@@ -278,6 +278,40 @@ hta_status hta_window_attn(const hta_dims *d, int32_t window, const hta_bf16 *q,
     p.dev_err = dev_err;
     if (hta::window_launch(p, pos, window, (int32_t)d->Lmax, stream) != cudaSuccess) return HTA_ERR_CUDA;
     g_last_path = kPathCC;
+    return HTA_OK;
+}
+
+hta_status hta_logitspec_tree(int32_t B, int32_t V, int64_t Lh_max, int32_t T, int32_t k, int32_t m,
+                              const float *logits, const int32_t *hist, const int32_t *hist_len,
+                              const int32_t *keep, int32_t *parents, int32_t *tokens, int32_t *n_nodes,
+                              int32_t *next_token, int32_t *dev_err, cudaStream_t stream) {
+    if (!logits || !hist || !hist_len || !keep || !parents || !tokens || !n_nodes || !next_token)
+        return HTA_ERR_INVALID_ARG;
+    if (B <= 0 || V <= 0 || T <= 0 || k < 0 || m <= 0 || Lh_max < 0) return HTA_ERR_INVALID_ARG;
+    if (k > HTA_LSPEC_KMAX || k + 1 > V || m < 2 || m > HTA_LSPEC_MMAX || T > HTA_TMAX || B > HTA_BMAX ||
+        Lh_max > (int64_t)0x7fffffff)
+        return HTA_ERR_UNSUPPORTED;
+    hta::LspecParams p;
+    memset(&p, 0, sizeof p);
+    for (int r = 0; r <= k; ++r) {
+        if (keep[r] < 0) return HTA_ERR_INVALID_ARG;
+        p.keep[r] = keep[r] < T ? keep[r] : T;
+    }
+    p.logits = logits;
+    p.hist = hist;
+    p.hist_len = hist_len;
+    p.parents = parents;
+    p.tokens = tokens;
+    p.n_nodes = n_nodes;
+    p.next_token = next_token;
+    p.dev_err = dev_err;
+    p.Lh_max = Lh_max;
+    p.B = B;
+    p.V = V;
+    p.T = T;
+    p.k = k;
+    p.m = m;
+    if (hta::lspec_launch(p, stream) != cudaSuccess) return HTA_ERR_CUDA;
     return HTA_OK;
 }
 

@@ -34,6 +34,20 @@ cudaError_t accept_launch(const int32_t *parents, const int32_t *draft, const in
 // draft-model sliding-window (W) self-attention over a ring of S slots (k_window.cu)
 cudaError_t window_launch(const AttnParams &p, const int32_t *pos, int32_t W, int32_t S, cudaStream_t stream);
 
+// LogitSpec draft-tree builder (k_lspec.cu)
+struct LspecParams {
+    const float *logits;       // [B][V]
+    const int32_t *hist;       // [B][Lh_max]
+    const int32_t *hist_len;   // [B]
+    int32_t *parents, *tokens;  // [B][T]
+    int32_t *n_nodes, *next_token;  // [B]
+    int32_t *dev_err;
+    int64_t Lh_max;
+    int32_t B, V, T, k, m;
+    int32_t keep[HTA_LSPEC_KMAX + 1];
+};
+cudaError_t lspec_launch(const LspecParams &p, cudaStream_t stream);
+
 // tree mask (k_mask.cu)
 cudaError_t mask_launch(const int32_t *parents, int B, int T, uint32_t *mask, int32_t *dev_err,
                         cudaStream_t stream);

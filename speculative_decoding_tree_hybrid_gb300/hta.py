@@ -30,7 +30,7 @@ TMAX, BMAX = 256, 1024
 # every exported symbol of include/hta.h
 EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
            "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn",
-           "hta_status_string",
+           "hta_logitspec_tree", "hta_status_string",
            "hta_last_path")
 
 
@@ -73,11 +73,12 @@ def load():
         lib.hta_verify_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_accept_commit.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_window_attn.argtypes = [D, I32, P, P, P, P, P, P, P, P]
+        lib.hta_logitspec_tree.argtypes = [I32, I32, I64, I32, I32, I32, P, P, P, P, P, P, P, P, P, P]
         lib.hta_status_string.argtypes = [ctypes.c_int]
         lib.hta_status_string.restype = ctypes.c_char_p
         lib.hta_last_path.restype = I32
         for name in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge", "hta_verify",
-                     "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn"):
+                     "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn", "hta_logitspec_tree"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -336,3 +337,36 @@ def window_attn(q, k_ring, v_ring, pos, window: int, *, scale: float = 0.0,
                                       _ptr(o), _ptr(lse), _ptr(dev_err), _stream(dev)),
                "hta_window_attn")
     return o, lse
+
+
+def logitspec_tree(logits, hist, hist_len, k: int, m: int, keep, T: int, *,
+                   dev_err: torch.Tensor | None = None, out: tuple | None = None):
+    """LogitSpec draft trees, one per sequence: logits fp32 [B][V], hist int32
+    [B][Lh_max] (the token stream), hist_len int32 [B]; keep: k + 1 ints (the
+    per-rank budget). Returns (parents int32 [B][T], tokens int32 [B][T],
+    n_nodes int32 [B], next_token int32 [B])."""
+    _check(logits, "logits", torch.float32, 2)
+    dev = logits.device
+    _check(hist, "hist", torch.int32, 2, dev)
+    _check(hist_len, "hist_len", torch.int32, 1, dev)
+    B, V = logits.shape
+    if hist.shape[0] != B or tuple(hist_len.shape) != (B,):
+        raise ValueError("hist must be [B][Lh_max] and hist_len [B]")
+    if len(keep) != k + 1:
+        raise ValueError("keep needs k + 1 entries")
+    keep_arr = (ctypes.c_int32 * (k + 1))(*[int(x) for x in keep])
+    if out is None:
+        parents = torch.empty((B, T), dtype=torch.int32, device=dev)
+        tokens = torch.empty((B, T), dtype=torch.int32, device=dev)
+        n_nodes = torch.empty((B,), dtype=torch.int32, device=dev)
+        nxt = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        parents, tokens, n_nodes, nxt = out
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_logitspec_tree(B, V, hist.shape[1], T, k, m, _ptr(logits), _ptr(hist), _ptr(hist_len),
+                                         keep_arr, _ptr(parents), _ptr(tokens), _ptr(n_nodes), _ptr(nxt),
+                                         _ptr(dev_err), _stream(dev)),
+               "hta_logitspec_tree")
+    return parents, tokens, n_nodes, nxt

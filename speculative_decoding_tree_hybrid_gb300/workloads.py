@@ -271,3 +271,62 @@ def window_inputs(B: int, T: int, Hq: int, Hkv: int, d: int, S: int, pos, *, see
         kr[b][:, js % S] = normal_bf16(rng, (Hkv, len(js), d))
         vr[b][:, js % S] = normal_bf16(rng, (Hkv, len(js), d))
     return WindowInputs(q, kr, vr, pos)
+
+
+# --------------------------------------------------------------------------- draft trees
+
+def token_stream(n: int, vocab: int, rng: np.random.Generator, copy_p: float = 0.6) -> np.ndarray:
+    """A token stream with the repetition that retrieval-based drafting relies
+    on: with probability copy_p the next span (2 to 16 tokens) copies an
+    earlier span of the stream, else one token is drawn uniformly."""
+    out = np.empty(n, dtype=np.int32)
+    fill = 0
+    while fill < n:
+        if fill > 8 and rng.random() < copy_p:
+            a = int(rng.integers(0, fill - 1))
+            ln = min(int(rng.integers(2, 17)), n - fill, fill - a)
+            out[fill:fill + ln] = out[a:a + ln]
+            fill += ln
+        else:
+            out[fill] = rng.integers(0, vocab)
+            fill += 1
+    return out
+
+
+def lspec_inputs(B: int, V: int, Lh: int, lens, *, seed: int, vocab_used: int | None = None,
+                 plant_m: int = 0, plant_guesses: int = 8):
+    """Logits N(0, 1) [B][V] (float32) and token streams [B][Lh] (int32, zero
+    past each length) with vocabulary vocab_used (default V).
+
+    plant_m > 0 stands in for a target model that favours tokens seen in the
+    context: the largest logit goes to a token that followed the stream's last
+    plant_m - 1 tokens earlier in the stream, and the next plant_guesses
+    logits to tokens that followed that token; the rest stay N(0, 1)."""
+    rng = np.random.default_rng(np.random.SeedSequence([3000, seed]))
+    lens = np.asarray(lens, dtype=np.int32).reshape(B)
+    logits = rng.standard_normal((B, V), dtype=np.float32)
+    hist = np.zeros((B, Lh), dtype=np.int32)
+    for b in range(B):
+        n = int(lens[b])
+        h = token_stream(n, vocab_used or V, rng)
+        hist[b, :n] = h
+        if plant_m <= 1 or n < plant_m:
+            continue
+        tail = h[n - (plant_m - 1):]
+        win = np.lib.stride_tricks.sliding_window_view(h[:n - 1], plant_m - 1)
+        hits = np.nonzero((win == tail).all(axis=1))[0]
+        hits = hits[hits + plant_m - 1 < n - 1]  # a token follows the earlier occurrence
+        if hits.size == 0:
+            continue
+        x1 = int(h[hits[-1] + plant_m - 1])
+        logits[b, x1] = 10.0
+        after = h[1:n][h[:n - 1] == x1]  # tokens that followed x1
+        seen = []
+        for t in after[::-1]:
+            if int(t) != x1 and int(t) not in seen:
+                seen.append(int(t))
+            if len(seen) == plant_guesses:
+                break
+        for r, t in enumerate(seen):
+            logits[b, t] = 9.0 - 0.1 * r
+    return logits, hist, lens

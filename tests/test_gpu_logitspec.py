@@ -1,0 +1,129 @@
+"""GPU parity of the LogitSpec draft-tree builder (hta_logitspec_tree) against
+oracle/logitspec.py ("LogitSpec: Accelerating Retrieval-based Speculative
+Decoding via Next Next Token Speculation", section 2): bit-exact parents,
+tokens, node counts and next tokens."""
+import json
+import pathlib
+
+import numpy as np
+import pytest
+
+from speculative_decoding_tree_hybrid_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from oracle.logitspec import build_trees  # noqa: E402
+from speculative_decoding_tree_hybrid_gb300 import build as hbuild  # noqa: E402
+from speculative_decoding_tree_hybrid_gb300 import hta  # noqa: E402
+
+hbuild.build()
+DEV = torch.device("cuda:0")
+CASES = json.loads((pathlib.Path(__file__).parent / "golden" / "logitspec_cases.json").read_text())["cases"]
+
+
+def run(logits, hist, lens, k, m, keep, T):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = hta.logitspec_tree(torch.from_numpy(np.ascontiguousarray(logits, np.float32)).to(DEV),
+                             torch.from_numpy(np.ascontiguousarray(hist, np.int32)).to(DEV),
+                             torch.from_numpy(np.ascontiguousarray(lens, np.int32)).to(DEV), k, m, keep, T,
+                             dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return [x.cpu().numpy() for x in out]
+
+
+def check(logits, hist, lens, k, m, keep, T):
+    par, tok, nn, nxt = run(logits, hist, lens, k, m, keep, T)
+    rp, rt, rn, rx = build_trees(logits, hist, lens, k, m, keep, T)
+    np.testing.assert_array_equal(nxt, rx)
+    np.testing.assert_array_equal(nn, rn)
+    np.testing.assert_array_equal(par, rp)
+    np.testing.assert_array_equal(tok, rt)
+    return nn
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c["name"] for c in CASES])
+def test_hand_derived_cases(case):
+    hist = np.array([case["hist"]], np.int32)
+    par, tok, nn, nxt = run(np.array([case["logits"]]), hist, [len(case["hist"])], case["k"], case["m"],
+                            case["keep"], case["T"])
+    assert par[0].tolist() == case["parents"] and tok[0].tolist() == case["tokens"]
+    assert nn[0] == case["n_nodes"] and nxt[0] == case["x_next"]
+
+
+# (B, V, Lh, k, m, T): small vocabularies (many matches), tiny and long
+# histories, every m, the largest k, trees cut short by T and T = 1
+SHAPES = [
+    (4, 50, 300, 5, 3, 32),
+    (8, 1000, 2000, 20, 2, 64),
+    (3, 80, 1000, 63, 4, 256),
+    (5, 300, 600, 10, 8, 40),
+    (2, 200, 50, 0, 3, 8),
+    (4, 64, 500, 7, 3, 1),
+    (6, 32000, 4096, 60, 3, 64),
+]
+
+
+@pytest.mark.parametrize("B,V,Lh,k,m,T", SHAPES)
+def test_trees_match_oracle(B, V, Lh, k, m, T):
+    rng = np.random.default_rng(B * 131 + V + k)
+    lens = rng.integers(0, Lh + 1, size=B)
+    lens[0] = Lh
+    logits, hist, lens = wl.lspec_inputs(B, V, Lh, lens, seed=B + V + Lh, vocab_used=min(V, 64))
+    keep = [int(x) for x in rng.integers(0, 12, size=k + 1)]
+    nn = check(logits, hist, lens, k, m, keep, T)
+    assert (nn >= 1).all()
+
+
+def test_tied_logits_take_smaller_ids():
+    # integer logits: long runs of ties across many 512-wide chunks
+    rng = np.random.default_rng(3)
+    B, V, Lh = 4, 20000, 400
+    logits = rng.integers(-2, 3, size=(B, V)).astype(np.float32)
+    logits[1] = 0.0  # every logit tied
+    logits[2, 12345] = 5.0
+    _, hist, lens = wl.lspec_inputs(B, V, Lh, [Lh] * B, seed=9, vocab_used=50)
+    check(logits, hist, lens, 63, 3, [3] * 64, 128)
+
+
+def test_nan_logits_rank_last():
+    B, V = 2, 100
+    logits = np.random.default_rng(4).standard_normal((B, V)).astype(np.float32)
+    logits[0, :50] = np.nan
+    _, hist, lens = wl.lspec_inputs(B, V, 200, [200, 0], seed=2, vocab_used=20)
+    check(logits, hist, lens, 10, 2, [4] * 11, 20)
+
+
+def test_full_size_vocab_and_history():
+    # LLaMA-3 vocabulary and a 32K-token history (two sequences keep the oracle
+    # quick), with logits that favour tokens of the context so retrieval hits
+    B, V, Lh = 2, 128256, 32768
+    logits, hist, lens = wl.lspec_inputs(B, V, Lh, [Lh, 20000], seed=11, vocab_used=4000, plant_m=3)
+    nn = check(logits, hist, lens, 60, 3, [16] + [max(1, 8 - r // 8) for r in range(1, 61)], 64)
+    # retrieved tokens fill the first tree past root + 60 guesses (the second
+    # stream's last 2-gram never occurred before, so it gets nothing to retrieve)
+    assert nn[0] == 64 and (nn >= 61).all()
+
+
+def test_random_logits_leave_only_guesses():
+    # no logit favours the context: nothing is retrieved, the tree is the root and the guesses
+    B, V, Lh = 2, 128256, 4096
+    logits, hist, lens = wl.lspec_inputs(B, V, Lh, [Lh, 100], seed=12, vocab_used=4000)
+    nn = check(logits, hist, lens, 60, 3, [16] * 61, 64)
+    assert (nn == 61).all()
+
+
+def test_bad_arguments():
+    x = torch.zeros((1, 10), dtype=torch.float32, device=DEV)
+    h = torch.zeros((1, 5), dtype=torch.int32, device=DEV)
+    ln = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    with pytest.raises(hta.HtaError):
+        hta.logitspec_tree(x, h, ln, 10, 3, [1] * 11, 8)  # k + 1 > V
+    with pytest.raises(hta.HtaError):
+        hta.logitspec_tree(x, h, ln, 2, 9, [1] * 3, 8)  # m > 8
+    with pytest.raises(hta.HtaError):
+        hta.logitspec_tree(x, h, ln, 2, 3, [1, -1, 1], 8)  # negative budget
