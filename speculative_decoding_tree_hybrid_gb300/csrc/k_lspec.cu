@@ -14,27 +14,36 @@
 // tokens after g2(r)'s match as a chain under it; nodes are added until T,
 // unused nodes are padding (parent 0, token -1).
 //
-// One CTA of 512 threads per sequence:
+// One cluster of 4 CTAs (512 threads each) per sequence; the leader CTA
+// holds the selection and the tree, the others add bandwidth:
 //  1. top-(k+1) of the logits by radix select on an order-preserving integer
-//     key: an 11-bit histogram of every key, then one pass keeping the keys
-//     above the chosen digit and moving the keys at it to shared memory
-//     (four 16-byte loads in flight per thread), where three more digits
+//     key: an 11-bit histogram of every key (each CTA a quarter of the
+//     logits, summed by the leader over distributed shared memory), then one
+//     pass keeping the keys above the chosen digit and moving the keys at it
+//     into the leader's shared memory (four 16-byte loads in flight per
+//     thread), where three more digits
 //     resolve the threshold; the keys above it and the smallest tied ids
 //     are the k+1 survivors, ranked by a counting sort (near-equal logits
 //     too many for shared memory resolve with passes over the logits);
 //  2. the 1 + k queries go into a hash table in shared memory (the pages'
-//     hash-based lookup) and every history position hashes its m-gram once,
-//     probes the table, confirms a hit token by token and keeps the latest
-//     start per query (atomicMax);
+//     hash-based lookup, copied to every CTA of the cluster) and every
+//     history position (a quarter per CTA) hashes its m-gram once, probes
+//     the table, confirms a hit token by token and keeps the latest start per
+//     query (atomicMax in the leader);
 //  3. branch sizes are laid out by one thread (at most 65 branches), then all
 //     threads write their nodes.
+#include <cooperative_groups.h>
+
 #include "hta_internal.cuh"
 #include "hta_launch.h"
+
+namespace cg = cooperative_groups;
 
 namespace hta {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kCtas = 4;  // CTAs per sequence: a thread-block cluster
 constexpr int kWarps = kThreads / 32;
 constexpr int kTable = 256;  // hash slots (at least twice the queries)
 constexpr int kEqCap = 512;  // threshold ties gathered in one pass (more: the ordered scan)
@@ -159,18 +168,25 @@ struct LspecSmem {
     int32_t remaining, sel_d, n_cand, n_buf, n_eq, eq_total, eq_base, n_nodes;
 };
 
-__global__ void __launch_bounds__(kThreads) k_logitspec_tree(const __grid_constant__ LspecParams p) {
+__global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
+    k_logitspec_tree(const __grid_constant__ LspecParams p) {
     __shared__ LspecSmem sm;
+    cg::cluster_group cl = cg::this_cluster();
+    const unsigned rank = cl.block_rank();
+    LspecSmem &lead = *cl.map_shared_rank(&sm, 0);  // the leader's shared memory
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x;
+    const int b = blockIdx.x / kCtas;
     const int K = p.k + 1, m = p.m;
     const float *lg = p.logits + (int64_t)b * p.V;
     const int32_t *hs = p.hist + (int64_t)b * p.Lh_max;
     int64_t n = p.hist_len[b];
     if (n < 0 || n > p.Lh_max) {
-        if (tid == 0) flag_error(p.dev_err, HTA_DEVERR_CACHE_LEN);
+        if (rank == 0 && tid == 0) flag_error(p.dev_err, HTA_DEVERR_CACHE_LEN);
         n = n < 0 ? 0 : p.Lh_max;
     }
+    // this CTA's slice of the logits (a multiple of 4 long: 16-byte loads stay aligned)
+    const int chunk = ((p.V + kCtas - 1) / kCtas + 3) & ~3;
+    const int v_lo = min(p.V, (int)rank * chunk), v_hi = min(p.V, v_lo + chunk);
 
     // ---- 1. the K largest keys: radix select of the K-th largest key.
     // Pass 0 histograms the top 11 bits of every key (global); one more global
@@ -187,32 +203,41 @@ __global__ void __launch_bounds__(kThreads) k_logitspec_tree(const __grid_consta
         sm.eq_base = 0;
     }
     __syncthreads();
-    for_each_key(lg, p.V, [&](int, uint32_t key) { atomicAdd(&h2k[key >> 21], 1u); });
-    __syncthreads();
-    select_digit(h2k, 2048, K, sm.wcount, &sm.sel_d, &sm.remaining);
-    if (tid == 0) {
-        sm.prefix = (uint32_t)sm.sel_d << 21;
-        sm.mask = 0xFFE00000u;
-        sm.eq_total = (int32_t)h2k[sm.sel_d];  // keys in the chosen digit
+    for_each_key(lg + v_lo, v_hi - v_lo, [&](int, uint32_t key) { atomicAdd(&h2k[key >> 21], 1u); });
+    cl.sync();  // every slice's histogram is complete
+    if (rank == 0) {
+        for (int i = tid; i < 2048; i += kThreads) {
+            uint32_t c = h2k[i];
+            for (unsigned r = 1; r < kCtas; ++r) c += cl.map_shared_rank(h2k, r)[i];
+            h2k[i] = c;
+        }
+        __syncthreads();
+        select_digit(h2k, 2048, K, sm.wcount, &sm.sel_d, &sm.remaining);
+        if (tid == 0) {
+            sm.prefix = (uint32_t)sm.sel_d << 21;
+            sm.mask = 0xFFE00000u;
+            sm.eq_total = (int32_t)h2k[sm.sel_d];  // keys in the chosen digit
+        }
     }
-    __syncthreads();
-    const bool in_smem = sm.eq_total <= kBuf;
+    cl.sync();  // the first digit is in the leader
+    const bool in_smem = lead.eq_total <= kBuf;
     {
-        const uint32_t d1 = sm.prefix >> 21;
-        for_each_key(lg, p.V, [&](int i, uint32_t key) {
+        const uint32_t d1 = lead.prefix >> 21;
+        for_each_key(lg + v_lo, v_hi - v_lo, [&](int i, uint32_t key) {
             const uint32_t top = key >> 21;
             if (top > d1) {
-                const int slot = atomicAdd(&sm.n_cand, 1);
-                sm.cand_key[slot] = key;
-                sm.cand_id[slot] = i;
+                const int slot = atomicAdd(&lead.n_cand, 1);
+                lead.cand_key[slot] = key;
+                lead.cand_id[slot] = v_lo + i;
             } else if (top == d1 && in_smem) {
-                const int slot = atomicAdd(&sm.n_buf, 1);
-                sm.buf_key[slot] = key;
-                sm.buf_id[slot] = i;
+                const int slot = atomicAdd(&lead.n_buf, 1);
+                lead.buf_key[slot] = key;
+                lead.buf_id[slot] = v_lo + i;
             }
         });
     }
-    __syncthreads();
+    cl.sync();  // every candidate is in the leader
+    if (rank == 0) {
     // the low 21 bits in three digits (8, 8, 5), over the buffer or the logits
     for (int pass = 0; pass < 3; ++pass) {
         const int shift = pass == 0 ? 13 : pass == 1 ? 5 : 0;
@@ -340,7 +365,7 @@ __global__ void __launch_bounds__(kThreads) k_logitspec_tree(const __grid_consta
     __syncthreads();
     const int32_t x1 = sm.top[0];
 
-    // ---- 2. queries into the hash table, one scan of the history
+    // ---- 2. queries into the hash table (leader), one scan of the history (cluster)
     for (int i = tid; i < kTable; i += kThreads) sm.slot_q[i] = -1;
     if (tid < K) {
         // query 0: the last m-1 history tokens and x1; query r: the last m-2, x1, guess r
@@ -361,21 +386,34 @@ __global__ void __launch_bounds__(kThreads) k_logitspec_tree(const __grid_consta
         while (atomicCAS(&sm.slot_q[s], -1, tid) != -1) s = (s + 1) & (kTable - 1);
         sm.slot_hash[s] = h;
     }
+    }  // leader
+    cl.sync();  // the queries and their table are in the leader
+    if (rank != 0) {  // a local copy of the table and the queries
+        for (int i = tid; i < kTable; i += kThreads) {
+            sm.slot_q[i] = lead.slot_q[i];
+            sm.slot_hash[i] = lead.slot_hash[i];
+        }
+        for (int i = tid; i < K * HTA_LSPEC_MMAX; i += kThreads) (&sm.q[0][0])[i] = (&lead.q[0][0])[i];
+    }
     __syncthreads();
-    // four positions per thread and iteration, their tokens loaded together
-    // into registers (a position's m-gram: the next m tokens, m <= 8)
-    for (int64_t s0 = tid; s0 + m <= n - 1; s0 += 4 * kThreads) {
+    // this CTA's quarter of the positions; four per thread and iteration,
+    // their tokens loaded together into registers (a position's m-gram: the
+    // next m tokens, m <= 8)
+    const int64_t n_pos = n - m > 0 ? n - m : 0;  // starts s with s + m <= n - 1
+    const int64_t pchunk = (n_pos + kCtas - 1) / kCtas;
+    const int64_t s_lo = min(n_pos, (int64_t)rank * pchunk), s_hi = min(n_pos, s_lo + pchunk);
+    for (int64_t s0 = s_lo + tid; s0 < s_hi; s0 += 4 * kThreads) {
         int32_t g[4][HTA_LSPEC_MMAX];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t s = s0 + (int64_t)u * kThreads;
 #pragma unroll
-            for (int j = 0; j < HTA_LSPEC_MMAX; ++j) g[u][j] = (j < m && s + m <= n - 1) ? __ldg(hs + s + j) : 0;
+            for (int j = 0; j < HTA_LSPEC_MMAX; ++j) g[u][j] = (j < m && s < s_hi) ? __ldg(hs + s + j) : 0;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t s = s0 + (int64_t)u * kThreads;
-            if (s + m > n - 1) continue;
+            if (s >= s_hi) continue;
             const uint32_t h = gram_hash(g[u], m);
             for (uint32_t t = h & (kTable - 1); sm.slot_q[t] >= 0; t = (t + 1) & (kTable - 1)) {
                 if (sm.slot_hash[t] != h) continue;
@@ -383,13 +421,15 @@ __global__ void __launch_bounds__(kThreads) k_logitspec_tree(const __grid_consta
                 bool same = true;
 #pragma unroll
                 for (int j = 0; j < HTA_LSPEC_MMAX; ++j) same = same && (j >= m || g[u][j] == sm.q[r][j]);
-                if (same) atomicMax(&sm.best[r], (int32_t)s);
+                if (same) atomicMax(&lead.best[r], (int32_t)s);
             }
         }
     }
-    __syncthreads();
+    cl.sync();  // every match is in the leader
+    if (rank != 0) return;
 
     // ---- 3. tree layout, then the nodes
+    const int32_t x1 = sm.top[0];
     if (tid == 0) {
         int32_t used = 1;  // the root
         for (int r = 0; r < K; ++r) {
@@ -440,7 +480,7 @@ __global__ void __launch_bounds__(kThreads) k_logitspec_tree(const __grid_consta
 }  // namespace
 
 cudaError_t lspec_launch(const LspecParams &p, cudaStream_t stream) {
-    k_logitspec_tree<<<p.B, kThreads, 0, stream>>>(p);
+    k_logitspec_tree<<<p.B * kCtas, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
