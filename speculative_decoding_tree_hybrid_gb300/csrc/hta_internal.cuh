@@ -433,6 +433,7 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                     const uint32_t t = r / G, hq = kvh * G + (r - t * G);
                     const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
                     const float *row0 = reinterpret_cast<const float *>(stage) + (uint32_t)i * REC;
+                    const int col0 = ch * 4;  // this thread's columns: col0 + 64 h + e, h < HPL / 4, e < 4
                     float M = -INFINITY;
                     for (int32_t k = 0; k < nrec; ++k)
                         if (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1])
@@ -450,7 +451,9 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                             den = fmaf(w, ml.y, den);
 #pragma unroll
                             for (int c = 0; c < HPL; c += 4) {
-                                const float4 v = *reinterpret_cast<const float4 *>(rec + ch * HPL + c);
+                                // columns 4 ch .. 4 ch + 3 of each 64-column half: the
+                                // lanes of a quarter-warp read 128 contiguous bytes
+                                const float4 v = *reinterpret_cast<const float4 *>(rec + col0 + c * 16);
                                 acc[c] = fmaf(w, v.x, acc[c]);
                                 acc[c + 1] = fmaf(w, v.y, acc[c + 1]);
                                 acc[c + 2] = fmaf(w, v.z, acc[c + 2]);
@@ -472,13 +475,13 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                         inv = 0.f;
                     }
                     if (out_fp32) {
-                        float *op = (float *)out_o + out_row * D + ch * HPL;
+                        float *op = (float *)out_o + out_row * D + col0;
 #pragma unroll
                         for (int c = 0; c < HPL; c += 4)
-                            *reinterpret_cast<float4 *>(op + c) =
+                            *reinterpret_cast<float4 *>(op + c * 16) =
                                 make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
                     } else {
-                        __nv_bfloat16 *op = (__nv_bfloat16 *)out_o + out_row * D + ch * HPL;
+                        __nv_bfloat16 *op = (__nv_bfloat16 *)out_o + out_row * D + col0;
 #pragma unroll
                         for (int c = 0; c < HPL; c += 4) {
                             const __nv_bfloat162 x = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
@@ -486,7 +489,7 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                             uint2 u;
                             u.x = *reinterpret_cast<const uint32_t *>(&x);
                             u.y = *reinterpret_cast<const uint32_t *>(&y);
-                            *reinterpret_cast<uint2 *>(op + c) = u;
+                            *reinterpret_cast<uint2 *>(op + c * 16) = u;
                         }
                     }
                     if (ch == 0) out_lse[out_row] = lse;
