@@ -432,12 +432,14 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
                     const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
                     const uint32_t t = r / G, hq = kvh * G + (r - t * G);
                     const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
-                    const float *row0 = reinterpret_cast<const float *>(stage) + (uint32_t)i * REC;
+                    // the staged records are read with shared-memory loads on their
+                    // shared-window address (a generic access costs a global-load latency)
+                    const uint32_t row0 = stage_u32 + (uint32_t)i * REC_BYTES;
                     const int col0 = ch * 4;  // this thread's columns: col0 + 64 h + e, h < HPL / 4, e < 4
                     float M = -INFINITY;
                     for (int32_t k = 0; k < nrec; ++k)
                         if (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1])
-                            M = fmaxf(M, row0[(uint32_t)k * pstride + D]);
+                            M = fmaxf(M, tc::lds_f32(row0 + ((uint32_t)k * pstride + D) * 4u));
                     float den = 0.f, acc[HPL];
 #pragma unroll
                     for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
@@ -445,15 +447,15 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
 #pragma unroll 2
                         for (int32_t k = 0; k < nrec; ++k) {
                             if (!dense && lo_s[cf + k / subs] == lo_s[cf + k / subs + 1]) continue;  // no record
-                            const float *rec = row0 + (uint32_t)k * pstride;
-                            const float2 ml = *reinterpret_cast<const float2 *>(rec + D);
+                            const uint32_t rec = row0 + (uint32_t)k * pstride * 4u;
+                            const float2 ml = tc::lds_f32x2(rec + D * 4u);
                             const float w = tc::ex2(ml.x - M);
                             den = fmaf(w, ml.y, den);
 #pragma unroll
                             for (int c = 0; c < HPL; c += 4) {
                                 // columns 4 ch .. 4 ch + 3 of each 64-column half: the
                                 // lanes of a quarter-warp read 128 contiguous bytes
-                                const float4 v = *reinterpret_cast<const float4 *>(rec + col0 + c * 16);
+                                const float4 v = tc::lds_f32x4(rec + (uint32_t)(col0 + c * 16) * 4u);
                                 acc[c] = fmaf(w, v.x, acc[c]);
                                 acc[c + 1] = fmaf(w, v.y, acc[c + 1]);
                                 acc[c + 2] = fmaf(w, v.z, acc[c + 2]);
