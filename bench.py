@@ -419,7 +419,7 @@ def run_gpu(args, world, rank, local, pg):
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "kv_sets": n_sets,
                    "l2": f"{n_sets} K/V caches of {bytes_step / 1e6:.1f} MB rotated (> 129 MB L2)",
-                   "graph": graph is not None, "path": {hta.PATH_TC: "tcgen05", hta.PATH_TC2: "tcgen05 2-CTA clusters"}.get(path, "cuda-core"),
+                   "graph": graph is not None, "path": {hta.PATH_TC: "tcgen05", hta.PATH_TC2: "tcgen05 CTA clusters"}.get(path, "cuda-core"),
                    "all_bytes_per_call": all_bytes(base)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

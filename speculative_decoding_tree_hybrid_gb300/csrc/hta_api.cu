@@ -64,9 +64,19 @@ int forced_path() {
 // pipeline of the tensor-core kernel (its 128-row tile has room to spare) than
 // through the CUDA-core kernel. Past 128 rows, pairs of SMs that share every
 // K/V tile (one 128-row half each), when 2-CTA clusters fit on the device.
+// CTAs per cluster of the clustered kernel: enough 128-row sub-groups (whole
+// tree nodes each) to hold every packed row of a KV head, 2 to 4; a larger
+// tree is split into row groups that each stream the cache
+int tc2_csize(const hta_dims *d) {
+    const int G = d->Hq / d->Hkv, nodes = hta::tc2_rows_per_sub() / G;  // tree nodes per CTA
+    if (nodes < 1) return 2;
+    const int need = (d->T + nodes - 1) / nodes;
+    return need < 2 ? 2 : need > 4 ? 4 : need;
+}
+
 bool tc2_fits(const hta_dims *d) {
-    const int G = d->Hq / d->Hkv;
-    return G <= 64 && hta::tc2_max_grid(d->B, num_sms_current()) >= 2;
+    const int G = d->Hq / d->Hkv, c = tc2_csize(d);
+    return G <= 64 && hta::tc2_max_grid(d->B, num_sms_current(), c) >= c;
 }
 
 int choose_path(const hta_dims *d) {
@@ -94,7 +104,7 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
     if (path == kPathTC2) {
         // whole tree nodes per group, each half of a group at most one
         // 128-row MMA tile
-        const int G = d->Hq / d->Hkv, tpg_max = 2 * (hta::tc2_rows_per_sub() / G);
+        const int G = d->Hq / d->Hkv, tpg_max = tc2_csize(d) * (hta::tc2_rows_per_sub() / G);
         L.n_rg = (d->T + tpg_max - 1) / tpg_max;
         L.rows_pg = (d->T + L.n_rg - 1) / L.n_rg * G;
     } else if (path == kPathTC) {
@@ -110,9 +120,9 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
     L.n_tree_tiles = tree ? (d->T + L.tile - 1) / L.tile : 0;
     L.n_seg = (int64_t)d->B * d->Hkv * L.n_rg;
     // record slots: (segment + worker) * records per piece, a staircase of
-    // pieces (the paired kernel has grid / 2 workers)
+    // pieces (the clustered kernel has grid / csize workers)
     L.subs = 1;
-    L.slots = (L.n_seg + (path == kPathTC2 ? grid / 2 : grid)) * L.subs;
+    L.slots = (L.n_seg + (path == kPathTC2 ? grid / tc2_csize(d) : grid)) * L.subs;
     // [barrier counters | partial records (d + 4 floats per row)]
     L.off_rec = kWsAlign;
     L.total = align_up(L.off_rec + (size_t)L.slots * L.rows_pg * (d->d + 4) * sizeof(float), kWsAlign);
@@ -122,7 +132,7 @@ Layout make_layout(const hta_dims *d, int path, int grid, bool tree) {
 int max_grid(int path, const hta_dims *d) {
     const int sms = num_sms_current();
     if (sms <= 0) return 0;
-    if (path == kPathTC2) return hta::tc2_max_grid(d->B, sms);
+    if (path == kPathTC2) return hta::tc2_max_grid(d->B, sms, tc2_csize(d));
     return path == kPathTC ? hta::tc_max_grid(d->B, sms) : hta::cc_max_grid(d->d, d->B, sms);
 }
 
@@ -168,13 +178,16 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
     if (path == kPathTC2 && direct) return HTA_ERR_UNSUPPORTED;  // tree-only calls take the CUDA-core path
     if (direct)
         grid = (int)(L0.n_seg < (int64_t)gmax ? L0.n_seg : gmax);
-    else if (path == kPathTC2)  // one worker per 2-CTA cluster
-        grid = 2 * (int)(max_units < (int64_t)(gmax / 2) ? (max_units > 0 ? max_units : 1) : gmax / 2);
+    else if (path == kPathTC2) {  // one worker per cluster
+        const int c = tc2_csize(d);
+        grid = c * (int)(max_units < (int64_t)(gmax / c) ? (max_units > 0 ? max_units : 1) : gmax / c);
+    }
     else
         grid = (int)(max_units < (int64_t)gmax ? (max_units > 0 ? max_units : 1) : gmax);
     Layout L = make_layout(d, path, grid, use_tree);
     AttnParams p = base_params(d, L);
-    p.workers = path == kPathTC2 ? grid / 2 : grid;
+    p.csize = path == kPathTC2 ? tc2_csize(d) : 0;
+    p.workers = path == kPathTC2 ? grid / p.csize : grid;
     p.q = (const __nv_bfloat16 *)q;
     p.k_cache = (const __nv_bfloat16 *)kc;
     p.v_cache = (const __nv_bfloat16 *)vc;

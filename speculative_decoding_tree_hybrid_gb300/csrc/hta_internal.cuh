@@ -65,6 +65,7 @@ struct AttnParams {
     // schedule: the unit space is split over `workers` (one CTA, or one
     // cluster of CTAs that share every tile)
     int32_t workers;
+    int32_t csize;  // CTAs per cluster of the clustered tensor-core kernel (2 .. 4)
     // partial records per (segment, worker) piece: a kernel may split a piece
     // over several softmax accumulators, each written as its own record
     int32_t subs;

@@ -22,7 +22,7 @@ cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream);
 // paired tcgen05 path, clusters of two CTAs sharing every K/V tile (k_tc2.cu)
 int tc2_tile();
 int tc2_rows_per_sub();
-int tc2_max_grid(int B, int num_sms);
+int tc2_max_grid(int B, int num_sms, int csize);
 cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream);
 
 // accept walk and KV commit (k_accept.cu)

@@ -59,7 +59,10 @@ constexpr uint32_t kSharedBytes = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;  // two O accumulators, alternating between pieces
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
-constexpr uint16_t kPair = 0x3;                  // both CTAs of the cluster
+constexpr int kMaxCluster = 4;                   // CTAs per cluster: 2 .. 4 (runtime)
+
+// every CTA of this cluster, as a multicast mask
+__device__ __forceinline__ uint16_t cluster_mask(const AttnParams &p) { return (uint16_t)((1u << p.csize) - 1u); }
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
 
@@ -90,7 +93,7 @@ struct SubGroup {
 __device__ __forceinline__ SubGroup sub_group(const AttnParams &p, uint32_t rank) {
     SubGroup s;
     s.tpg = p.rows_pg / p.G;
-    s.tph = (s.tpg + 1) >> 1;
+    s.tph = (s.tpg + p.csize - 1) / p.csize;
     s.t0 = (int32_t)rank * s.tph;
     return s;
 }
@@ -142,8 +145,9 @@ __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh
         mbar_arrive_expect_tx_if(leader, full, kTileBytes);
         if ((uint32_t)is_v == rank) {
             const CUtensorMap *map = tree ? (is_v ? &maps.vs : &maps.ks) : (is_v ? &maps.vc : &maps.kc);
-            tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, kPair, policy);
-            tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, kPair, policy);
+            tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, cluster_mask(p), policy);
+            tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, cluster_mask(p),
+                                policy);
         }
         ++j;
     }
@@ -212,7 +216,7 @@ __device__ __forceinline__ bool issue_s(const AttnParams &p, Tc2Shared &sh, vola
     tc_fence_after();
     issue_qk(leader, tmem + (j & 1) * 128, q_desc0 + ((qb * kQBufBytes) >> 4), k_desc0 + ((st * kTileBytes) >> 4));
     mma_commit(leader, bar_addr(sh.s_full[j & 1]));
-    mma_commit_mc(leader, bar_addr(sh.empty[st]), kPair);
+    mma_commit_mc(leader, bar_addr(sh.empty[st]), cluster_mask(p));
     if (t.last) mma_commit(leader, bar_addr(sh.q_empty[qb]));
     return true;
 }
@@ -245,7 +249,7 @@ __device__ void mma_issuer(const AttnParams &p, Tc2Shared &sh, uint32_t sQ, uint
         tc_fence_after();
         issue_pv(leader, tmem + kColO + (cur.q & 1) * 128, tmem + b * 128, v_desc0 + ((stv * kTileBytes) >> 4),
                  !cur.first);
-        mma_commit_mc(leader, bar_addr(sh.empty[stv]), kPair);
+        mma_commit_mc(leader, bar_addr(sh.empty[stv]), cluster_mask(p));
         mma_commit(leader, bar_addr(sh.pv_done[b]));
         if (has2 && !issue_s<kStages>(p, sh, abort, leader, i + 2, n2, tmem, q_desc0, k_desc0)) return;
         if (!has1) break;
@@ -489,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every cluster operation below (multicast copies and commits, cluster
     // barriers) assumes a cluster of exactly two CTAs and one worker per
     // cluster; a launch in any other shape writes nothing and says so.
-    if (cluster_nctarank() != 2 || gridDim.x != 2u * (uint32_t)p.workers || (gridDim.x & 1u)) {
+    if (p.csize < 2 || p.csize > kMaxCluster || cluster_nctarank() != (uint32_t)p.csize ||
+        gridDim.x != (uint32_t)p.csize * (uint32_t)p.workers) {
         if (threadIdx.x == 0) flag_error(p.dev_err, HTA_DEVERR_LAUNCH);
         return;
     }
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_addr(sh.full[s]), 1);
-            mbar_init(bar_addr(sh.empty[s]), 2);
+            mbar_init(bar_addr(sh.empty[s]), (uint32_t)p.csize);  // the MMA warp of every CTA
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_addr(sh.s_full[b]), 1);
@@ -577,7 +582,7 @@ int tc2_stages(int B, int workers) {
 
 template <int kStages>
 cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cudaStream_t stream) {
-    const size_t smem = tc2_smem_bytes(kStages, p.B, grid / 2);
+    const size_t smem = tc2_smem_bytes(kStages, p.B, grid / p.csize);
     cudaError_t e = cudaFuncSetAttribute(k_tc2_verify<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -589,7 +594,7 @@ cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cu
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.x = (unsigned)p.csize;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -598,18 +603,18 @@ cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cu
 }
 
 template <int kStages>
-int max_clusters(int B, int num_sms) {
+int max_clusters(int B, int num_sms, int csize) {
     const size_t smem = tc2_smem_bytes(kStages, B, num_sms / 2);
     if (cudaFuncSetAttribute(k_tc2_verify<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((num_sms / 2) * 2);
+    cfg.gridDim = dim3((num_sms / csize) * csize);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = (unsigned)csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -624,30 +629,32 @@ int max_clusters(int B, int num_sms) {
 int tc2_tile() { return kTile; }
 int tc2_rows_per_sub() { return kSubRows; }
 
-// CTAs of the largest co-resident grid of 2-CTA clusters (0 if none); the
-// occupancy query runs once per device and ring depth
-int tc2_max_grid(int B, int num_sms) {
+// CTAs of the largest co-resident grid of csize-CTA clusters (0 if none); the
+// occupancy query runs once per device, ring depth and cluster size
+int tc2_max_grid(int B, int num_sms, int csize) {
+    if (csize < 2 || csize > kMaxCluster) return 0;
     const int stages = tc2_stages(B, num_sms / 2);
     if (stages == 0) return 0;
     static std::mutex mu;
-    static int cached[64][2];  // [device][stages == 5], 0 = not yet queried
+    static int cached[64][2][kMaxCluster + 1];  // [device][stages == 5][csize], 0 = not yet queried
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    int &n = cached[dev][stages == 5 ? 1 : 0];
-    if (n == 0) n = 1 + (stages == 5 ? max_clusters<5>(B, num_sms) : max_clusters<4>(B, num_sms));
+    int &n = cached[dev][stages == 5 ? 1 : 0][csize];
+    if (n == 0) n = 1 + (stages == 5 ? max_clusters<5>(B, num_sms, csize) : max_clusters<4>(B, num_sms, csize));
     const int clusters = n - 1;
-    return 2 * (clusters < num_sms / 2 ? clusters : num_sms / 2);
+    return csize * (clusters < num_sms / csize ? clusters : num_sms / csize);
 }
 
 cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     Tc2Maps maps;
     memset(&maps, 0, sizeof maps);
     const int64_t heads = (int64_t)p.B * p.Hkv;
-    if (grid < 2 || grid % 2 != 0 || p.workers != grid / 2) return cudaErrorInvalidValue;
+    if (p.csize < 2 || p.csize > kMaxCluster || grid < p.csize || grid % p.csize != 0 || p.workers != grid / p.csize)
+        return cudaErrorInvalidValue;
     // row groups of whole tree nodes, each half at most 128 rows
     if (p.G < 1 || p.rows_pg % p.G != 0) return cudaErrorInvalidValue;
-    const int tpg = p.rows_pg / p.G, tph = (tpg + 1) / 2;
+    const int tpg = p.rows_pg / p.G, tph = (tpg + p.csize - 1) / p.csize;
     if (tph * p.G > kSubRows) return cudaErrorInvalidValue;
     if (!tch::encode_q(&maps.q, p.q, p.B, p.T, p.Hq, p.G, tph)) return cudaErrorInvalidValue;
     if (!tch::encode_kv(&maps.kc, p.k_cache, p.Lmax, heads, kTile) ||
@@ -656,7 +663,7 @@ cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     if (p.include_tree &&
         (!tch::encode_kv(&maps.ks, p.k_spec, p.T, heads, kTile) || !tch::encode_kv(&maps.vs, p.v_spec, p.T, heads, kTile)))
         return cudaErrorInvalidValue;
-    const int stages = tc2_stages(p.B, grid / 2);
+    const int stages = tc2_stages(p.B, grid / p.csize);
     if (stages == 5) return launch_stages<5>(p, maps, grid, stream);
     if (stages == 4) return launch_stages<4>(p, maps, grid, stream);
     return cudaErrorInvalidConfiguration;

@@ -122,6 +122,8 @@ SMALL = [
     (2, 33, 10, 2, 128, [128, 256], "uniform"),     # G = 5, T not a multiple of 32
     (1, 100, 16, 4, 128, [900], "window8_depth8"),  # two row groups of 200 rows (two 100-row halves)
     (1, 65, 16, 4, 128, [600], "uniform"),          # short last row group, odd nodes per group
+    (1, 64, 64, 8, 128, [777], "window8_depth8"),   # G = 8: 512 rows, clusters of four CTAs
+    (3, 64, 40, 8, 128, [300, 1029, 0], "window8_depth8"),  # QwQ shape, ragged incl. an empty cache
 ]
 
 
