@@ -63,7 +63,8 @@ int forced_path() {
 // (a few packed rows per KV head) streams the cache faster through the TMA
 // pipeline of the tensor-core kernel (its 128-row tile has room to spare) than
 // through the CUDA-core kernel. Past 128 rows, pairs of SMs that share every
-// K/V tile (one 128-row half each), when 2-CTA clusters fit on the device.
+// K/V tile (one 128-row sub-group each, 2 to 4 per cluster), when such
+// clusters fit on the device.
 // CTAs per cluster of the clustered kernel: enough 128-row sub-groups (whole
 // tree nodes each) to hold every packed row of a KV head, 2 to 4; a larger
 // tree is split into row groups that each stream the cache

@@ -19,7 +19,7 @@ int tc_tile();
 int tc_max_grid(int B, int num_sms);
 cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream);
 
-// paired tcgen05 path, clusters of two CTAs sharing every K/V tile (k_tc2.cu)
+// clustered tcgen05 path, clusters of 2 to 4 CTAs sharing every K/V tile (k_tc2.cu)
 int tc2_tile();
 int tc2_rows_per_sub();
 int tc2_max_grid(int B, int num_sms, int csize);

@@ -9,17 +9,18 @@
 // tiles of one persistent cooperative grid and the cross-split merge runs
 // after a grid barrier in the same launch.
 //
-// Here the grid is made of clusters of two CTAs on two SMs. A cluster owns a
-// range of tiles of the static split-KV schedule; a row group (up to 256
-// packed rows of one KV head, whole tree nodes) is split into two sub-groups
-// of at most 128 rows, one per CTA. Each K/V tile is read from HBM once per
-// cluster: CTA 0 loads the K tiles and CTA 1 the V tiles, each TMA copy
-// multicast into both CTAs' rings, and a ring stage is refilled only after
-// the MMAs of both CTAs have released it. With one 128-row sub-group per SM,
+// Here the grid is made of clusters of csize CTAs (2 to 4) on csize SMs. A
+// cluster owns a range of tiles of the static split-KV schedule; a row group
+// (up to csize x 128 packed rows of one KV head, whole tree nodes) is split
+// into csize sub-groups of at most 128 rows, one per CTA. Each K/V tile is
+// read from HBM once per cluster: CTA 0 loads the K tiles and CTA 1 the V
+// tiles, each TMA copy multicast into every CTA's ring, and a ring stage is
+// refilled only after the MMAs of every CTA have released it. With one
+// 128-row sub-group per SM,
 // tensor memory holds two S buffers next to O, so S(i+1) is computed while
 // the softmax works on tile i and the softmax runs tile after tile:
-//   warps 0, 3  TMA producers of the K ring and the V ring (this CTA's half of
-//               the copies, multicast to the pair)
+//   warps 0, 3  TMA producers of the K ring and the V ring (CTA 0 issues the
+//               K copies, CTA 1 the V copies, multicast to the cluster)
 //   warp 1      MMA issuer: S(i) = Q K(i)^T into S[i % 2], O += P(i) V(i)
 //   warp 2      TMA loads of each piece's Q rows (double-buffered)
 //   warps 4-7   softmax, one query row per thread
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = smem_u32(smem + kOffQ), ring = smem_u32(smem + kOffRing);
     const int warp = threadIdx.x >> 5;
     // Every cluster operation below (multicast copies and commits, cluster
-    // barriers) assumes a cluster of exactly two CTAs and one worker per
+    // barriers) assumes a cluster of exactly csize CTAs and one worker per
     // cluster; a launch in any other shape writes nothing and says so.
     if (p.csize < 2 || p.csize > kMaxCluster || cluster_nctarank() != (uint32_t)p.csize ||
         gridDim.x != (uint32_t)p.csize * (uint32_t)p.workers) {
