@@ -76,7 +76,7 @@ struct Tc2Maps {
 
 struct Tc2Shared {
     uint64_t full[kMaxStages];
-    uint64_t empty[kMaxStages];  // two arrivals: the MMA warps of both CTAs
+    uint64_t empty[kMaxStages];  // csize arrivals: the MMA warp of every CTA
     uint64_t s_full[2], p_full[2], pv_done[2], o_free[2], q_full[2], q_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -118,7 +118,7 @@ __device__ __forceinline__ uint32_t ring_round(bool is_v, uint32_t j) {
 
 // One producer warp per ring. Both CTAs expect the bytes of every tile on
 // their own barrier; CTA 0 issues the K copies and CTA 1 the V copies, each
-// multicast to both CTAs.
+// multicast to every CTA of the cluster.
 template <int kStages>
 __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh, uint32_t ring, uint32_t rank,
                          bool is_v, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
@@ -137,7 +137,7 @@ __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
         const int z = t.b * p.Hkv + t.kvh;
         const uint32_t st = ring_stage<kStages>(is_v, j), round = ring_round<kStages>(is_v, j);
-        // free in both CTAs (and the previous round of full[st] is complete here)
+        // free in every CTA (and the previous round of full[st] is complete here)
         if (!wait_warp(bar_addr(sh.empty[st]), (round & 1) ^ 1, abort, p.dev_err)) {
             ok = false;
             break;
@@ -204,7 +204,7 @@ __device__ __forceinline__ void issue_pv(uint32_t leader, uint32_t o_tmem, uint3
 }
 
 // S(j) into S[j % 2]: waits for K(j) and, at the start of a piece, for its
-// Q rows; releases K(j) in both CTAs and, after the last S of a piece, the
+// Q rows; releases K(j) in every CTA and, after the last S of a piece, the
 // piece's Q buffer
 template <int kStages>
 __device__ __forceinline__ bool issue_s(const AttnParams &p, Tc2Shared &sh, volatile int32_t *abort,
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     }
     build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
-    // both CTAs' barriers exist before either multicasts into the other
+    // every CTA's barriers exist before any multicasts into another
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
