@@ -116,8 +116,8 @@ __device__ __forceinline__ uint32_t ring_round(bool is_v, uint32_t j) {
     return is_v ? j / (kStages - kKStages) : j / kKStages;
 }
 
-// One producer warp per ring. Both CTAs expect the bytes of every tile on
-// their own barrier; CTA 0 issues the K copies and CTA 1 the V copies, each
+// One producer warp per ring. Every CTA expects the bytes of every tile on
+// its own barrier; CTA 0 issues the K copies and CTA 1 the V copies, each
 // multicast to every CTA of the cluster.
 template <int kStages>
 __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh, uint32_t ring, uint32_t rank,
