@@ -276,6 +276,14 @@ def run_reference(args, world, rank, pg):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def parse_kv_layout(text: str):
+    """'hnd' | 'nhd' | '<order>:<page tokens>' -> (order, page_size or 0)."""
+    order, _, page = text.partition(":")
+    if order not in ("hnd", "nhd"):
+        raise SystemExit(f"--kv-layout: order must be hnd or nhd, got {order!r}")
+    return order, int(page) if page else 0
+
+
 def run_gpu(args, world, rank, local, pg):
     import torch
 
@@ -297,9 +305,26 @@ def run_gpu(args, world, rank, local, pg):
     ks, vs = bf16(base.k_spec), bf16(base.v_spec)
     lens = torch.from_numpy(base.cache_lens).to(dev)
     parents = torch.from_numpy(base.parents).to(dev)
-    kcs = [bf16(s.k_cache) for s in sets]
-    vcs = [bf16(s.v_cache) for s in sets]
-    dims = hta.dims_of(q, kcs[0])
+    order, page = parse_kv_layout(args.kv_layout)
+    tables = [None] * n_sets
+    if page:  # every set scattered into its own pool of pages
+        kcs, vcs = [], []
+        for k, s in enumerate(sets):
+            kp, vp, tb = wl.paged_kv(s.k_cache, s.v_cache, s.cache_lens, page, order=order, seed=k)
+            kcs.append(bf16(kp))
+            vcs.append(bf16(vp))
+            tables[k] = torch.from_numpy(tb).to(dev)
+    elif order == "nhd":
+        kcs = [bf16(wl.kv_nhd(s.k_cache)) for s in sets]
+        vcs = [bf16(wl.kv_nhd(s.v_cache)) for s in sets]
+    else:
+        kcs = [bf16(s.k_cache) for s in sets]
+        vcs = [bf16(s.v_cache) for s in sets]
+    if order == "nhd":
+        ks, vs = bf16(wl.kv_nhd(base.k_spec)), bf16(wl.kv_nhd(base.v_spec))
+    default_layout = order == "hnd" and not page
+    Lmax = page * tables[0].shape[1] if page else base.Lmax
+    dims = hta.HtaDims(cfg.B, cfg.T, cfg.Hq, cfg.Hkv, cfg.d, int(Lmax), 0.0)
     ws = hta.workspace(dims, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     o = torch.empty_like(q)
@@ -308,9 +333,16 @@ def run_gpu(args, world, rank, local, pg):
 
     stream = torch.cuda.Stream(dev)
 
+    def verify_call(k):
+        if default_layout:
+            hta.verify(q, kcs[k], vcs[k], lens, ks, vs, mask, ws=ws, dev_err=err, out=(o, lse))
+        else:
+            hta.verify_kv(q, kcs[k], vcs[k], lens, ks, vs, mask, order=order, block_table=tables[k], ws=ws,
+                          dev_err=err, out=(o, lse))
+
     def one_step(k):
         hta.build_mask(parents, dev_err=err, out=mask)
-        hta.verify(q, kcs[k], vcs[k], lens, ks, vs, mask, ws=ws, dev_err=err, out=(o, lse))
+        verify_call(k)
 
     # one graph replays one step per K/V set
     graph = None
@@ -359,7 +391,7 @@ def run_gpu(args, world, rank, local, pg):
             flush.fill_(i & 0xFF)
             hta.build_mask(parents, dev_err=err, out=mask)
             ev[i][0].record(stream)
-            hta.verify(q, kcs[k], vcs[k], lens, ks, vs, mask, ws=ws, dev_err=err, out=(o, lse))
+            verify_call(k)
             ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
@@ -386,8 +418,8 @@ def run_gpu(args, world, rank, local, pg):
     bytes_step = kv_bytes(base)
     gbs, t_max = aggregate(bytes_step * steps / 1e9, elapsed, pg, dev)
 
-    # end to end through the public API with host buffers
-    e2e = run_e2e(args, hta, sets, dev, pg)
+    # end to end through the public API with host buffers (contiguous layout)
+    e2e = run_e2e(args, hta, sets, dev, pg) if default_layout else None
 
     if rank != 0:
         return
@@ -418,6 +450,7 @@ def run_gpu(args, world, rank, local, pg):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "kv_sets": n_sets,
+                   "kv_layout": ("contiguous " if not page else f"{page}-token pages, ") + order,
                    "l2": f"{n_sets} K/V caches of {bytes_step / 1e6:.1f} MB rotated (> 129 MB L2)",
                    "graph": graph is not None, "path": {hta.PATH_TC: "tcgen05", hta.PATH_TC2: "tcgen05 CTA clusters"}.get(path, "cuda-core"),
                    "all_bytes_per_call": all_bytes(base)},
@@ -751,6 +784,9 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--kv-layout", default="hnd",
+                    help="cache storage for --op verify: hnd (default, contiguous head-major), nhd "
+                         "(token-major), or <order>:<page tokens> for a paged pool, e.g. nhd:16")
     ap.add_argument("--op", choices=["verify", "accept", "cross", "window", "lspec"], default="verify",
                     help="verify: the hot path (default); accept: the accept walk + K/V append step alone; "
                          "cross / window: the draft model's cross-attention / sliding-window attention; "

@@ -47,6 +47,32 @@ hta_status check_dims(const hta_dims *d) {
     return HTA_OK;
 }
 
+// The storage rules of hta_kv_layout; NULL = contiguous head-major.
+hta_status check_layout(const hta_dims *d, const hta_kv_layout *l) {
+    if (!l) return HTA_OK;
+    if (l->order != HTA_KV_HND && l->order != HTA_KV_NHD) return HTA_ERR_INVALID_ARG;
+    if (l->page_size < 0) return HTA_ERR_INVALID_ARG;
+    if (l->page_size == 0) return HTA_OK;
+    const int32_t P = l->page_size;
+    // a 128-key tile covers whole pages, or lies inside one
+    if (!(P == 16 || P == 32 || P == 64 || P % 128 == 0)) return HTA_ERR_INVALID_ARG;
+    if (!l->block_table || l->max_pages <= 0 || l->num_pages <= 0) return HTA_ERR_INVALID_ARG;
+    if (d->Lmax > (int64_t)l->max_pages * P) return HTA_ERR_INVALID_ARG;
+    return HTA_OK;
+}
+
+void apply_layout(AttnParams &p, const hta_kv_layout *l) {
+    if (!l) return;
+    p.kv_nhd = l->order == HTA_KV_NHD ? 1 : 0;
+    p.page_size = l->page_size;
+    if (l->page_size > 0) {
+        p.max_pages = l->max_pages;
+        p.num_pages = l->num_pages;
+        p.block_table = l->block_table;
+    }
+    p.kv_generic = (p.kv_nhd || p.page_size > 0) ? 1 : 0;
+}
+
 enum Path { kPathNone = 0, kPathCC = 1, kPathTC = 2, kPathTC2 = 3 };
 
 // Environment override HTA_FORCE_PATH=cc|tc|tc2, read on every call.
@@ -163,7 +189,8 @@ AttnParams base_params(const hta_dims *d, const Layout &L) {
 hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const void *vc,
                          const int32_t *lens, const void *ks, const void *vs, const uint32_t *mask,
                          void *out_o, float *out_lse, bool out_fp32, bool use_cache, bool use_tree,
-                         void *ws, size_t ws_bytes, int32_t *dev_err, cudaStream_t stream) {
+                         void *ws, size_t ws_bytes, int32_t *dev_err, cudaStream_t stream,
+                         const hta_kv_layout *kvl = nullptr) {
     const int path = choose_path(d);
     if (path == kPathNone) return HTA_ERR_UNSUPPORTED;
     const int gmax = max_grid(path, d);
@@ -202,6 +229,7 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
     p.include_cache = use_cache ? 1 : 0;
     p.include_tree = use_tree ? 1 : 0;
     p.dev_err = dev_err;
+    apply_layout(p, kvl);
     if (!direct) {
         if (!ws || ((uintptr_t)ws % kWsAlign) != 0 || ws_bytes < L.total) return HTA_ERR_WORKSPACE;
         char *base = (char *)ws;
@@ -256,16 +284,36 @@ hta_status hta_accept_commit(const hta_dims *d, const int32_t *parents, const in
                              hta_bf16 *k_cache, hta_bf16 *v_cache, int32_t *cache_lens, int32_t *accepted,
                              int32_t *n_accepted, int32_t *next_token, int32_t *dev_err,
                              cudaStream_t stream) {
+    return hta_accept_commit_kv(d, nullptr, parents, draft, target, k_spec, v_spec, k_cache, v_cache, cache_lens,
+                                accepted, n_accepted, next_token, dev_err, stream);
+}
+
+hta_status hta_accept_commit_kv(const hta_dims *d, const hta_kv_layout *layout, const int32_t *parents,
+                                const int32_t *draft, const int32_t *target, const hta_bf16 *k_spec,
+                                const hta_bf16 *v_spec, hta_bf16 *k_cache, hta_bf16 *v_cache, int32_t *cache_lens,
+                                int32_t *accepted, int32_t *n_accepted, int32_t *next_token, int32_t *dev_err,
+                                cudaStream_t stream) {
     if (!d || !parents || !draft || !target || !k_spec || !v_spec || !k_cache || !v_cache || !cache_lens ||
         !accepted || !n_accepted || !next_token)
         return HTA_ERR_INVALID_ARG;
     if (d->B <= 0 || d->T <= 0 || d->Hkv <= 0 || d->d <= 0 || d->Lmax < 0) return HTA_ERR_INVALID_ARG;
     if (d->d != 64 && d->d != 128) return HTA_ERR_UNSUPPORTED;
     if (d->T > HTA_TMAX || d->B > HTA_BMAX || d->Lmax > (int64_t)0x7fffffff) return HTA_ERR_UNSUPPORTED;
+    if (check_layout(d, layout) != HTA_OK) return HTA_ERR_INVALID_ARG;
     if (!aligned16(k_spec) || !aligned16(v_spec) || !aligned16(k_cache) || !aligned16(v_cache))
         return HTA_ERR_ALIGN;
+    hta::KvStore st = {};
+    if (layout) {
+        st.nhd = layout->order == HTA_KV_NHD ? 1 : 0;
+        st.page_size = layout->page_size;
+        if (layout->page_size > 0) {
+            st.max_pages = layout->max_pages;
+            st.num_pages = layout->num_pages;
+            st.block_table = layout->block_table;
+        }
+    }
     if (hta::accept_launch(parents, draft, target, d->B, d->T, d->Hkv, d->d, d->Lmax, k_spec, v_spec, k_cache,
-                           v_cache, cache_lens, accepted, n_accepted, next_token, dev_err, stream) != cudaSuccess)
+                           v_cache, cache_lens, accepted, n_accepted, next_token, dev_err, st, stream) != cudaSuccess)
         return HTA_ERR_CUDA;
     return HTA_OK;
 }
@@ -412,6 +460,36 @@ hta_status hta_verify(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k_ca
         return HTA_ERR_ALIGN;
     return run_attention(d, q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, o, lse, false,
                          true, true, workspace, workspace_bytes, dev_err, stream);
+}
+
+hta_status hta_verify_kv(const hta_dims *d, const hta_kv_layout *layout, const hta_bf16 *q,
+                         const hta_bf16 *k_cache, const hta_bf16 *v_cache, const int32_t *cache_lens,
+                         const hta_bf16 *k_spec, const hta_bf16 *v_spec, const uint32_t *mask, hta_bf16 *o,
+                         float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_err,
+                         cudaStream_t stream) {
+    hta_status s = check_dims(d);
+    if (s != HTA_OK) return s;
+    if ((s = check_layout(d, layout)) != HTA_OK) return s;
+    if (!q || !k_cache || !v_cache || !cache_lens || !k_spec || !v_spec || !mask || !o || !lse)
+        return HTA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_spec) ||
+        !aligned16(v_spec) || !aligned16(o))
+        return HTA_ERR_ALIGN;
+    return run_attention(d, q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, o, lse, false,
+                         true, true, workspace, workspace_bytes, dev_err, stream, layout);
+}
+
+hta_status hta_prefix_attn_kv(const hta_dims *d, const hta_kv_layout *layout, const hta_bf16 *q,
+                              const hta_bf16 *k_cache, const hta_bf16 *v_cache, const int32_t *cache_lens,
+                              float *o_c, float *lse_c, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_err, cudaStream_t stream) {
+    hta_status s = check_dims(d);
+    if (s != HTA_OK) return s;
+    if ((s = check_layout(d, layout)) != HTA_OK) return s;
+    if (!q || !k_cache || !v_cache || !cache_lens || !o_c || !lse_c) return HTA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_c)) return HTA_ERR_ALIGN;
+    return run_attention(d, q, k_cache, v_cache, cache_lens, nullptr, nullptr, nullptr, o_c, lse_c,
+                         true, true, false, workspace, workspace_bytes, dev_err, stream, layout);
 }
 
 }  // extern "C"

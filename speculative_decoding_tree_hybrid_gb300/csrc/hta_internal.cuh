@@ -69,6 +69,13 @@ struct AttnParams {
     // partial records per (segment, worker) piece: a kernel may split a piece
     // over several softmax accumulators, each written as its own record
     int32_t subs;
+    // K/V storage: kv_nhd = the Hkv heads of a token are adjacent
+    // ([..][rows][Hkv][d], cache and tree), else rows of a head are
+    // ([..][Hkv][rows][d]); page_size 0 = one block of Lmax rows per
+    // sequence, else pool pages of page_size rows named by block_table
+    // [B][max_pages]. kv_generic: anything but contiguous head-major.
+    int32_t kv_nhd, page_size, max_pages, num_pages, kv_generic;
+    const int32_t *block_table;
 };
 
 // ---------------------------------------------------------------- errors
@@ -86,6 +93,30 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ---------------------------------------------------------------- K/V rows
+
+// Element offset of cache token j of sequence b, KV head kvh. A block-table
+// entry outside the pool is flagged and read as page 0.
+__device__ __forceinline__ int64_t cache_row_off(const AttnParams &p, int32_t b, int32_t kvh, int32_t j) {
+    if (p.page_size == 0)
+        return p.kv_nhd ? (((int64_t)b * p.Lmax + j) * p.Hkv + kvh) * p.d
+                        : (((int64_t)b * p.Hkv + kvh) * p.Lmax + j) * p.d;
+    int32_t pg = __ldg(p.block_table + (int64_t)b * p.max_pages + j / p.page_size);
+    if (pg < 0 || pg >= p.num_pages) {
+        flag_error(p.dev_err, HTA_DEVERR_PAGE);
+        pg = 0;
+    }
+    const int32_t r = j % p.page_size;
+    return p.kv_nhd ? (((int64_t)pg * p.page_size + r) * p.Hkv + kvh) * p.d
+                    : (((int64_t)pg * p.Hkv + kvh) * p.page_size + r) * p.d;
+}
+
+// Element offset of tree token j of sequence b, KV head kvh.
+__device__ __forceinline__ int64_t spec_row_off(const AttnParams &p, int32_t b, int32_t kvh, int32_t j) {
+    return p.kv_nhd ? (((int64_t)b * p.T + j) * p.Hkv + kvh) * p.d
+                    : (((int64_t)b * p.Hkv + kvh) * p.T + j) * p.d;
 }
 
 // ---------------------------------------------------------------- schedule

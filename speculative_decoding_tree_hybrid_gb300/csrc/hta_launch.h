@@ -25,11 +25,16 @@ int tc2_rows_per_sub();
 int tc2_max_grid(int B, int num_sms, int csize);
 cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream);
 
-// accept walk and KV commit (k_accept.cu)
+// accept walk and KV commit (k_accept.cu); `st` is the cache storage (all
+// zero: contiguous head-major)
+struct KvStore {
+    int32_t nhd, page_size, max_pages, num_pages;
+    const int32_t *block_table;
+};
 cudaError_t accept_launch(const int32_t *parents, const int32_t *draft, const int32_t *target, int B, int T,
                           int Hkv, int d, int64_t Lmax, const void *k_spec, const void *v_spec, void *k_cache,
                           void *v_cache, int32_t *cache_lens, int32_t *accepted, int32_t *n_accepted,
-                          int32_t *next_token, int32_t *dev_err, cudaStream_t stream);
+                          int32_t *next_token, int32_t *dev_err, const KvStore &st, cudaStream_t stream);
 
 // draft-model sliding-window (W) self-attention over a ring of S slots (k_window.cu)
 cudaError_t window_launch(const AttnParams &p, const int32_t *pos, int32_t W, int32_t S, cudaStream_t stream);

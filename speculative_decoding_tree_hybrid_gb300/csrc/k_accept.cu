@@ -14,7 +14,10 @@
 //
 // One CTA per sequence. Warp 0 walks the tree from shared memory, 32
 // candidate children per ballot; then all threads copy the path's rows in
-// 16-byte chunks, eight loads in flight per thread.
+// 16-byte chunks, eight loads in flight per thread. kGeneric: the cache (and
+// the tree's K/V) in another storage than contiguous head-major (token-major
+// rows, pool pages named by a block table); a row whose page entry lies
+// outside the pool is not written and flags HTA_DEVERR_PAGE.
 #include "hta_launch.h"
 
 namespace hta {
@@ -23,12 +26,24 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatch = 8;
 
+// Row index (in rows of d elements) of cache token pos of (b, h) under `st`;
+// -1 when its page entry lies outside the pool.
+__device__ __forceinline__ int64_t store_row(const KvStore &st, int b, int h, int64_t pos, int Hkv, int64_t Lmax) {
+    if (st.page_size == 0)
+        return st.nhd ? ((int64_t)b * Lmax + pos) * Hkv + h : ((int64_t)b * Hkv + h) * Lmax + pos;
+    const int32_t pg = __ldg(st.block_table + (int64_t)b * st.max_pages + pos / st.page_size);
+    if (pg < 0 || pg >= st.num_pages) return -1;
+    const int64_t r = pos % st.page_size;
+    return st.nhd ? ((int64_t)pg * st.page_size + r) * Hkv + h : ((int64_t)pg * Hkv + h) * st.page_size + r;
+}
+
+template <bool kGeneric>
 __global__ void __launch_bounds__(kThreads)
     k_accept_commit(const int32_t *__restrict__ parents, const int32_t *__restrict__ draft,
                     const int32_t *__restrict__ target, int T, int Hkv, int d, int64_t Lmax,
                     const uint4 *__restrict__ k_spec, const uint4 *__restrict__ v_spec, uint4 *k_cache,
                     uint4 *v_cache, int32_t *cache_lens, int32_t *accepted, int32_t *n_accepted,
-                    int32_t *next_token, int32_t *dev_err) {
+                    int32_t *next_token, int32_t *dev_err, const KvStore st) {
     __shared__ int32_t par_s[HTA_TMAX], tok_s[HTA_TMAX], tgt_s[HTA_TMAX], path_s[HTA_TMAX];
     __shared__ int32_t n_s, len_s;
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -91,8 +106,19 @@ __global__ void __launch_bounds__(kThreads)
                 const int kv = x >= per_kv, y = x - kv * per_kv;
                 const int h = y / (nc * cpr), r = y - h * nc * cpr, j = r / cpr, ch = r - j * cpr;
                 const int64_t head = (int64_t)b * Hkv + h;
-                v[u] = (kv ? v_spec : k_spec)[(head * T + path_s[j]) * cpr + ch];
-                dst[u] = ((head * Lmax + L + j) * cpr + ch) * 2 + kv;  // chunk index, K/V in bit 0
+                if constexpr (!kGeneric) {
+                    v[u] = (kv ? v_spec : k_spec)[(head * T + path_s[j]) * cpr + ch];
+                    dst[u] = ((head * Lmax + L + j) * cpr + ch) * 2 + kv;  // chunk index, K/V in bit 0
+                } else {
+                    const int64_t src = st.nhd ? ((int64_t)b * T + path_s[j]) * Hkv + h : head * T + path_s[j];
+                    const int64_t row = store_row(st, b, h, (int64_t)L + j, Hkv, Lmax);
+                    if (row >= 0) {
+                        v[u] = (kv ? v_spec : k_spec)[src * cpr + ch];
+                        dst[u] = (row * cpr + ch) * 2 + kv;
+                    } else if (ch == 0 && kv == 0) {
+                        flag_error(dev_err, HTA_DEVERR_PAGE);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -108,10 +134,15 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t accept_launch(const int32_t *parents, const int32_t *draft, const int32_t *target, int B, int T,
                           int Hkv, int d, int64_t Lmax, const void *k_spec, const void *v_spec, void *k_cache,
                           void *v_cache, int32_t *cache_lens, int32_t *accepted, int32_t *n_accepted,
-                          int32_t *next_token, int32_t *dev_err, cudaStream_t stream) {
-    k_accept_commit<<<B, kThreads, 0, stream>>>(parents, draft, target, T, Hkv, d, Lmax, (const uint4 *)k_spec,
-                                                 (const uint4 *)v_spec, (uint4 *)k_cache, (uint4 *)v_cache,
-                                                 cache_lens, accepted, n_accepted, next_token, dev_err);
+                          int32_t *next_token, int32_t *dev_err, const KvStore &st, cudaStream_t stream) {
+    if (st.nhd || st.page_size > 0)
+        k_accept_commit<true><<<B, kThreads, 0, stream>>>(
+            parents, draft, target, T, Hkv, d, Lmax, (const uint4 *)k_spec, (const uint4 *)v_spec, (uint4 *)k_cache,
+            (uint4 *)v_cache, cache_lens, accepted, n_accepted, next_token, dev_err, st);
+    else
+        k_accept_commit<false><<<B, kThreads, 0, stream>>>(
+            parents, draft, target, T, Hkv, d, Lmax, (const uint4 *)k_spec, (const uint4 *)v_spec, (uint4 *)k_cache,
+            (uint4 *)v_cache, cache_lens, accepted, n_accepted, next_token, dev_err, st);
     return cudaGetLastError();
 }
 

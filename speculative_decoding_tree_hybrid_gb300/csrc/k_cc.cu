@@ -53,9 +53,13 @@ __device__ __forceinline__ void cc_piece(const AttnParams &p, CcSmem<D> &sm, int
         for (int i = tid; i < kTile * (D / 8); i += kThreads) {
             const int j = i / (D / 8), c8 = (i % (D / 8)) * 8;
             uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
-            if (j < nvalid) {
+            if (j < nvalid && !p.kv_generic) {
                 kr = __ldg(reinterpret_cast<const uint4 *>(kg + (int64_t)j * D + c8));
                 vr = __ldg(reinterpret_cast<const uint4 *>(vg + (int64_t)j * D + c8));
+            } else if (j < nvalid) {  // token-major or paged storage: row by row
+                const int64_t off = (tree ? spec_row_off(p, b, kvh, j0 + j) : cache_row_off(p, b, kvh, j0 + j)) + c8;
+                kr = __ldg(reinterpret_cast<const uint4 *>((tree ? p.k_spec : p.k_cache) + off));
+                vr = __ldg(reinterpret_cast<const uint4 *>((tree ? p.v_spec : p.v_cache) + off));
             }
             *reinterpret_cast<uint4 *>(&sm.k[j][c8]) = kr;
             *reinterpret_cast<uint4 *>(&sm.v[j][c8]) = vr;

@@ -82,7 +82,7 @@ static_assert(sizeof(TcShared) <= kSharedBytes, "shared control block too large"
 
 // ------------------------------------------------------------------ roles
 
-template <int kStages>
+template <int kStages, bool kGeneric>
 __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, uint32_t ring,
                          const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
@@ -95,6 +95,7 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
     const uint32_t leader = elect_one();
     // K and V are streamed once: keep them from evicting everything else in L2
     const uint64_t policy = l2_evict_first_policy();
+    [[maybe_unused]] PageWindow pw;  // paged layouts only
     while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
@@ -108,8 +109,14 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
             const CUtensorMap *map = tree ? (kv ? &maps.vs : &maps.ks) : (kv ? &maps.vc : &maps.kc);
             const uint32_t full = bar_addr(sh.full[st]);
             mbar_arrive_expect_tx_if(leader, full, kTileBytes);
-            tma_load_3d_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, policy);
-            tma_load_3d_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, policy);
+            if constexpr (!kGeneric) {
+                tma_load_3d_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, policy);
+                tma_load_3d_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, policy);
+            } else {
+                kv_tile_4d(p, pw, tree, t.b, t.kvh, y, t.Lb, [&](uint32_t off, int c0, int c1, int c2, int c3) {
+                    tma_load_4d_hint(leader, ring + st * kTileBytes + off, map, full, c0, c1, c2, c3, policy);
+                });
+            }
         }
     }
     if (!ok) {
@@ -394,7 +401,9 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
     }
 }
 
-template <int kStages>
+// kGeneric: K/V stored in any layout but contiguous head-major (4-D maps,
+// paged pools)
+template <int kStages, bool kGeneric = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_verify(const __grid_constant__ AttnParams p, const __grid_constant__ TcMaps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -450,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
         if (warp == 0)
-            producer<kStages>(p, maps, sh, ring, lens_s, pre_s, u0, u1);
+            producer<kStages, kGeneric>(p, maps, sh, ring, lens_s, pre_s, u0, u1);
         else if (warp == 1)
             mma_issuer<kStages>(p, sh, sQ, ring, tmem, halves, lens_s, pre_s, u0, u1);
         else if (warp == 2)
@@ -496,10 +505,10 @@ int tc_stages(int B, int grid) {
     return 0;
 }
 
-template <int kStages>
+template <int kStages, bool kGeneric>
 cudaError_t launch_stages(const AttnParams &p, const TcMaps &maps, int grid, cudaStream_t stream) {
     const size_t smem = tc_smem_bytes(kStages, p.B, grid);
-    cudaError_t e = cudaFuncSetAttribute(k_tc_verify<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_tc_verify<kStages, kGeneric>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -511,7 +520,7 @@ cudaError_t launch_stages(const AttnParams &p, const TcMaps &maps, int grid, cud
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_tc_verify<kStages>, p, maps);
+    return cudaLaunchKernelEx(&cfg, k_tc_verify<kStages, kGeneric>, p, maps);
 }
 
 }  // namespace
@@ -543,14 +552,14 @@ cudaError_t tc_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     // row groups must be whole tree nodes (rows_pg = tpg * G, tpg <= 256)
     if (p.G < 1 || p.rows_pg % p.G != 0 || p.rows_pg > kMaxRows) return cudaErrorInvalidValue;
     if (!tch::encode_q(&maps.q, p.q, p.B, p.T, p.Hq, p.G, p.rows_pg / p.G)) return cudaErrorInvalidValue;
-    if (!tch::encode_kv(&maps.kc, p.k_cache, p.Lmax, heads, kTile) || !tch::encode_kv(&maps.vc, p.v_cache, p.Lmax, heads, kTile))
-        return cudaErrorInvalidValue;
-    if (p.include_tree &&
-        (!tch::encode_kv(&maps.ks, p.k_spec, p.T, heads, kTile) || !tch::encode_kv(&maps.vs, p.v_spec, p.T, heads, kTile)))
-        return cudaErrorInvalidValue;
+    if (!tch::encode_kv_maps(p, heads, kTile, &maps.kc, &maps.vc, &maps.ks, &maps.vs)) return cudaErrorInvalidValue;
     const int stages = tc_stages(p.B, grid);
-    if (stages == 5) return launch_stages<5>(p, maps, grid, stream);
-    if (stages == 4) return launch_stages<4>(p, maps, grid, stream);
+    if (stages == 5)
+        return p.kv_generic ? launch_stages<5, true>(p, maps, grid, stream)
+                            : launch_stages<5, false>(p, maps, grid, stream);
+    if (stages == 4)
+        return p.kv_generic ? launch_stages<4, true>(p, maps, grid, stream)
+                            : launch_stages<4, false>(p, maps, grid, stream);
     return cudaErrorInvalidConfiguration;
 }
 

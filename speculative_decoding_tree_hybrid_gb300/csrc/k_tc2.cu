@@ -119,7 +119,7 @@ __device__ __forceinline__ uint32_t ring_round(bool is_v, uint32_t j) {
 // One producer warp per ring. Every CTA expects the bytes of every tile on
 // its own barrier; CTA 0 issues the K copies and CTA 1 the V copies, each
 // multicast to every CTA of the cluster.
-template <int kStages>
+template <int kStages, bool kGeneric>
 __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh, uint32_t ring, uint32_t rank,
                          bool is_v, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
     volatile int32_t *abort = &sh.abort;
@@ -132,6 +132,7 @@ __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh
     bool ok = true;
     const uint32_t leader = elect_one();
     const uint64_t policy = l2_evict_first_policy();  // K and V are read once
+    [[maybe_unused]] PageWindow pw;  // paged layouts only
     while (ok && cursor_next(c, p, lens_s, pre_s, t)) {
         const bool tree = t.unit < n_tree;
         const int y = (tree ? t.unit : t.unit - n_tree) * kTile;
@@ -146,9 +147,16 @@ __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh
         mbar_arrive_expect_tx_if(leader, full, kTileBytes);
         if ((uint32_t)is_v == rank) {
             const CUtensorMap *map = tree ? (is_v ? &maps.vs : &maps.ks) : (is_v ? &maps.vc : &maps.kc);
-            tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, cluster_mask(p), policy);
-            tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, cluster_mask(p),
-                                policy);
+            if constexpr (!kGeneric) {
+                tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, cluster_mask(p), policy);
+                tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z,
+                                    cluster_mask(p), policy);
+            } else {
+                kv_tile_4d(p, pw, tree, t.b, t.kvh, y, t.Lb, [&](uint32_t off, int c0, int c1, int c2, int c3) {
+                    tma_load_4d_mc_hint(leader, ring + st * kTileBytes + off, map, full, c0, c1, c2, c3,
+                                        cluster_mask(p), policy);
+                });
+            }
         }
         ++j;
     }
@@ -478,7 +486,9 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
     if (pend.on && ok) write_record(4);
 }
 
-template <int kStages>
+// kGeneric: K/V stored in any layout but contiguous head-major (4-D maps,
+// paged pools)
+template <int kStages, bool kGeneric = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc2_verify(const __grid_constant__ AttnParams p, const __grid_constant__ Tc2Maps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -541,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u0 = lo_s[worker], u1 = lo_s[worker + 1];
 
     if (warp == 0 || warp == 3)
-        producer<kStages>(p, maps, sh, ring, rank, warp == 3, lens_s, pre_s, u0, u1);
+        producer<kStages, kGeneric>(p, maps, sh, ring, rank, warp == 3, lens_s, pre_s, u0, u1);
     else if (warp == 1)
         mma_issuer<kStages>(p, sh, sQ, ring, tmem, lens_s, pre_s, u0, u1);
     else if (warp == 2)
@@ -581,10 +591,10 @@ int tc2_stages(int B, int workers) {
     return 0;
 }
 
-template <int kStages>
+template <int kStages, bool kGeneric>
 cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cudaStream_t stream) {
     const size_t smem = tc2_smem_bytes(kStages, p.B, grid / p.csize);
-    cudaError_t e = cudaFuncSetAttribute(k_tc2_verify<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_tc2_verify<kStages, kGeneric>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -600,7 +610,7 @@ cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cu
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_tc2_verify<kStages>, p, maps);
+    return cudaLaunchKernelEx(&cfg, k_tc2_verify<kStages, kGeneric>, p, maps);
 }
 
 template <int kStages>
@@ -658,15 +668,14 @@ cudaError_t tc2_launch(const AttnParams &p, int grid, cudaStream_t stream) {
     const int tpg = p.rows_pg / p.G, tph = (tpg + p.csize - 1) / p.csize;
     if (tph * p.G > kSubRows) return cudaErrorInvalidValue;
     if (!tch::encode_q(&maps.q, p.q, p.B, p.T, p.Hq, p.G, tph)) return cudaErrorInvalidValue;
-    if (!tch::encode_kv(&maps.kc, p.k_cache, p.Lmax, heads, kTile) ||
-        !tch::encode_kv(&maps.vc, p.v_cache, p.Lmax, heads, kTile))
-        return cudaErrorInvalidValue;
-    if (p.include_tree &&
-        (!tch::encode_kv(&maps.ks, p.k_spec, p.T, heads, kTile) || !tch::encode_kv(&maps.vs, p.v_spec, p.T, heads, kTile)))
-        return cudaErrorInvalidValue;
+    if (!tch::encode_kv_maps(p, heads, kTile, &maps.kc, &maps.vc, &maps.ks, &maps.vs)) return cudaErrorInvalidValue;
     const int stages = tc2_stages(p.B, grid / p.csize);
-    if (stages == 5) return launch_stages<5>(p, maps, grid, stream);
-    if (stages == 4) return launch_stages<4>(p, maps, grid, stream);
+    if (stages == 5)
+        return p.kv_generic ? launch_stages<5, true>(p, maps, grid, stream)
+                            : launch_stages<5, false>(p, maps, grid, stream);
+    if (stages == 4)
+        return p.kv_generic ? launch_stages<4, true>(p, maps, grid, stream)
+                            : launch_stages<4, false>(p, maps, grid, stream);
     return cudaErrorInvalidConfiguration;
 }
 

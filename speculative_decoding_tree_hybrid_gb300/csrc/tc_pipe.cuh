@@ -92,5 +92,76 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const AttnParams &p, cons
     return true;
 }
 
+// ------------------------------------------------------------ K/V layouts
+
+// Block-table entries of one producer warp: lane i holds entry base + i of
+// sequence b and, in `next`, entry base + 32 + i. Moving on to the next 32
+// entries uses `next` and loads the 32 after it, so that load has a window's
+// worth of tiles to land; only a jump (a new sequence) waits for a load.
+struct PageWindow {
+    int32_t b = -1, base = 0, entry = 0, next = 0;
+};
+
+__device__ __forceinline__ int32_t table_entry(const AttnParams &p, int32_t b, int32_t s) {
+    return s < p.max_pages ? __ldg(p.block_table + (int64_t)b * p.max_pages + s) : 0;
+}
+
+// Pool page of cache token j of sequence b. Warp-collective: every lane
+// calls it with the same (b, j). An entry outside the pool is flagged and
+// read as page 0.
+__device__ __forceinline__ int32_t page_of(const AttnParams &p, PageWindow &w, int32_t b, int32_t j) {
+    const int32_t slot = j / p.page_size, lane = (int32_t)(threadIdx.x & 31);
+    if (b != w.b || slot < w.base || slot >= w.base + 64) {
+        w.b = b;
+        w.base = slot;
+        w.entry = table_entry(p, b, slot + lane);
+        w.next = table_entry(p, b, slot + 32 + lane);
+    } else if (slot >= w.base + 32) {
+        w.base += 32;
+        w.entry = w.next;
+        w.next = table_entry(p, b, w.base + 32 + lane);
+    }
+    int32_t pg = __shfl_sync(0xffffffffu, w.entry, slot - w.base);
+    if (pg < 0 || pg >= p.num_pages) {
+        if (lane == 0) flag_error(p.dev_err, HTA_DEVERR_PAGE);
+        pg = 0;
+    }
+    return pg;
+}
+
+// Copies of one 128-key K or V tile whose first key is y (a cache token, or
+// a tree token when `tree`), for every layout but contiguous head-major,
+// through 4-D tensor maps: head-major (d, rows, Hkv, outer), token-major
+// (d, Hkv, rows, outer), outer = the sequence or the pool page. One box per
+// 64-dim half and per page the tile spans (boxes of min(page_size, 128)
+// rows); a box past the sequence's last page reads page 0 (those keys are
+// masked and their V rows cleared like any key past the end).
+// load4(shared-memory offset in the tile, c0, c1, c2, c3) issues one box.
+template <typename Load4>
+__device__ __forceinline__ void kv_tile_4d(const AttnParams &p, PageWindow &w, bool tree, int32_t b, int32_t kvh,
+                                           int32_t y, int32_t Lb, Load4 &&load4) {
+    constexpr uint32_t kHalf = 128 * 64 * 2;  // one 64-dim half of a tile
+    if (tree || p.page_size == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (p.kv_nhd) load4(h * kHalf, h * 64, kvh, y, b);
+            else load4(h * kHalf, h * 64, y, kvh, b);
+        }
+        return;
+    }
+    const int32_t rows = p.page_size < 128 ? p.page_size : 128;
+    for (int32_t r = 0; r < 128; r += rows) {
+        const int32_t j = y + r;
+        const int32_t pg = j < Lb ? page_of(p, w, b, j) : 0;
+        const int32_t row = j % p.page_size;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t off = h * kHalf + (uint32_t)r * 128;
+            if (p.kv_nhd) load4(off, h * 64, kvh, row, pg);
+            else load4(off, h * 64, row, kvh, pg);
+        }
+    }
+}
+
 }  // namespace tcp
 }  // namespace hta

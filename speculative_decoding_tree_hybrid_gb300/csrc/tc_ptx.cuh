@@ -163,6 +163,33 @@ __device__ __forceinline__ void tma_load_3d_mc_hint(uint32_t leader, uint32_t ds
         : "memory");
 }
 
+// 4-D tiled load with an L2 cache policy
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t leader, uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int x, int y, int z, int w, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%1], [%2, {%4, %5, %6, %7}], [%3], %8;\n\t}" ::"r"(leader),
+        "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+        : "memory");
+}
+
+// tma_load_4d_hint multicast to the CTAs of `mask` in this cluster (as
+// tma_load_3d_mc_hint)
+__device__ __forceinline__ void tma_load_4d_mc_hint(uint32_t leader, uint32_t dst, const CUtensorMap *map,
+                                                    uint32_t bar, int x, int y, int z, int w, uint16_t mask,
+                                                    uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %0, 0;\n\t"
+        "@q cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%1], [%2, {%4, %5, %6, %7}], [%3], %8, %9;\n\t}" ::"r"(leader),
+        "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask),
+        "l"(policy)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing on `bar` (16-byte aligned
 // addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

@@ -24,13 +24,15 @@ _lib = None
 _ws_cache: dict = {}
 
 PATH_CC, PATH_TC, PATH_TC2 = 1, 2, 3
-DEVERR_BAD_TREE, DEVERR_CACHE_LEN, DEVERR_TIMEOUT, DEVERR_LAUNCH = 1, 2, 4, 8
+DEVERR_BAD_TREE, DEVERR_CACHE_LEN, DEVERR_TIMEOUT, DEVERR_LAUNCH, DEVERR_PAGE = 1, 2, 4, 8, 16
+KV_HND, KV_NHD = 0, 1
 TMAX, BMAX = 256, 1024
 
 # every exported symbol of include/hta.h
 EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
            "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn",
-           "hta_logitspec_tree", "hta_status_string",
+           "hta_logitspec_tree", "hta_verify_kv", "hta_prefix_attn_kv", "hta_accept_commit_kv",
+           "hta_status_string",
            "hta_last_path")
 
 
@@ -44,6 +46,11 @@ class HtaDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hq", ctypes.c_int32),
                 ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("Lmax", ctypes.c_int64),
                 ("scale", ctypes.c_float)]
+
+
+class HtaKvLayout(ctypes.Structure):
+    _fields_ = [("order", ctypes.c_int32), ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("block_table", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -74,6 +81,10 @@ def load():
         lib.hta_accept_commit.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_window_attn.argtypes = [D, I32, P, P, P, P, P, P, P, P]
         lib.hta_logitspec_tree.argtypes = [I32, I32, I64, I32, I32, I32, P, P, P, P, P, P, P, P, P, P]
+        KL = ctypes.POINTER(HtaKvLayout)
+        lib.hta_verify_kv.argtypes = [D, KL, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+        lib.hta_prefix_attn_kv.argtypes = [D, KL, P, P, P, P, P, P, P, SZ, P, P]
+        lib.hta_accept_commit_kv.argtypes = [D, KL, P, P, P, P, P, P, P, P, P, P, P, P, P]
         lib.hta_status_string.argtypes = [ctypes.c_int]
         lib.hta_status_string.restype = ctypes.c_char_p
         lib.hta_last_path.restype = I32
@@ -235,6 +246,97 @@ def prefix_attn(q, k_cache, v_cache, cache_lens, *, scale: float = 0.0,
     return o_c, lse_c
 
 
+def _kv_layout(q, k_cache, v_cache, cache_lens, order: str, block_table):
+    """Checks a cache stored as `order` ("hnd" or "nhd"), contiguous
+    (block_table None: [B][Hkv][Lmax][d] or [B][Lmax][Hkv][d]) or paged
+    (a pool [pages][Hkv][P][d] or [pages][P][Hkv][d] and block_table int32
+    [B][max_pages]). Returns (dims, HtaKvLayout, Hkv)."""
+    if order not in ("hnd", "nhd"):
+        raise ValueError("order must be 'hnd' or 'nhd'")
+    nhd = order == "nhd"
+    _check(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    _check(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _check(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _check(cache_lens, "cache_lens", torch.int32, 1, dev)
+    B, T, Hq, d = q.shape
+    if v_cache.shape != k_cache.shape or k_cache.shape[3] != d:
+        raise ValueError("k_cache/v_cache must have the same shape, head dimension last")
+    if cache_lens.shape[0] != B:
+        raise ValueError("cache_lens must be [B]")
+    rows, Hkv = (k_cache.shape[1], k_cache.shape[2]) if nhd else (k_cache.shape[2], k_cache.shape[1])
+    lay = HtaKvLayout(KV_NHD if nhd else KV_HND, 0, 0, 0, None)
+    if block_table is None:
+        if k_cache.shape[0] != B:
+            raise ValueError("a contiguous cache has one block of Lmax rows per sequence")
+        Lmax = rows
+    else:
+        _check(block_table, "block_table", torch.int32, 2, dev)
+        if block_table.shape[0] != B:
+            raise ValueError("block_table must be [B][max_pages]")
+        lay.page_size, lay.max_pages, lay.num_pages = rows, block_table.shape[1], k_cache.shape[0]
+        lay.block_table = block_table.data_ptr()
+        Lmax = rows * block_table.shape[1]
+    return HtaDims(B, T, Hq, Hkv, d, Lmax, 0.0), lay, Hkv
+
+
+def verify_kv(q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, *, order: str = "hnd",
+              block_table: torch.Tensor | None = None, scale: float = 0.0,
+              ws: torch.Tensor | None = None, dev_err: torch.Tensor | None = None,
+              out: tuple | None = None):
+    """verify() over a token-major and/or paged cache (see _kv_layout);
+    k_spec/v_spec are [B][Hkv][T][d] ("hnd") or [B][T][Hkv][d] ("nhd").
+    Returns (o bf16 [B][T][Hq][d], lse fp32 [B][T][Hq])."""
+    dims, lay, Hkv = _kv_layout(q, k_cache, v_cache, cache_lens, order, block_table)
+    dims.scale = float(scale)
+    B, T, Hq, d = q.shape
+    dev = q.device
+    _check(k_spec, "k_spec", torch.bfloat16, 4, dev)
+    _check(v_spec, "v_spec", torch.bfloat16, 4, dev)
+    _check(mask, "mask", torch.int32, 3, dev)
+    want = (B, T, Hkv, d) if order == "nhd" else (B, Hkv, T, d)
+    if tuple(k_spec.shape) != want or v_spec.shape != k_spec.shape:
+        raise ValueError(f"k_spec/v_spec must be {want}")
+    if tuple(mask.shape) != (B, T, (T + 31) // 32):
+        raise ValueError("mask must be [B][T][ceil(T/32)]")
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    else:
+        o, lse = out
+    if ws is None:
+        ws = workspace(dims, dev)
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_verify_kv(ctypes.byref(dims), ctypes.byref(lay), _ptr(q), _ptr(k_cache),
+                                    _ptr(v_cache), _ptr(cache_lens), _ptr(k_spec), _ptr(v_spec), _ptr(mask),
+                                    _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_err), _stream(dev)),
+               "hta_verify_kv")
+    return o, lse
+
+
+def prefix_attn_kv(q, k_cache, v_cache, cache_lens, *, order: str = "hnd",
+                   block_table: torch.Tensor | None = None, scale: float = 0.0,
+                   ws: torch.Tensor | None = None, dev_err: torch.Tensor | None = None):
+    """prefix_attn() over a token-major and/or paged cache (see _kv_layout).
+    Returns (o_c fp32 [B][T][Hq][d], lse_c fp32 [B][T][Hq])."""
+    dims, lay, _ = _kv_layout(q, k_cache, v_cache, cache_lens, order, block_table)
+    dims.scale = float(scale)
+    dev = q.device
+    o_c = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse_c = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(dims, dev)
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_prefix_attn_kv(ctypes.byref(dims), ctypes.byref(lay), _ptr(q), _ptr(k_cache),
+                                         _ptr(v_cache), _ptr(cache_lens), _ptr(o_c), _ptr(lse_c), _ptr(ws),
+                                         ws.numel(), _ptr(dev_err), _stream(dev)), "hta_prefix_attn_kv")
+    return o_c, lse_c
+
+
 def tree_attn(q, k_spec, v_spec, mask, *, scale: float = 0.0):
     """Speculative part alone. Returns (o_s fp32 [B][T][Hq][d], lse_s fp32 [B][T][Hq])."""
     _check(q, "q", torch.bfloat16, 4)
@@ -306,6 +408,61 @@ def accept_commit(parents, draft, target, k_spec, v_spec, k_cache, v_cache, cach
                                         _ptr(cache_lens), _ptr(accepted), _ptr(n_acc), _ptr(nxt),
                                         _ptr(dev_err) if dev_err is not None else None, _stream(dev)),
                "hta_accept_commit")
+    return accepted, n_acc, nxt
+
+
+def accept_commit_kv(parents, draft, target, k_spec, v_spec, k_cache, v_cache, cache_lens, *,
+                     order: str = "hnd", block_table: torch.Tensor | None = None,
+                     dev_err: torch.Tensor | None = None, out=None):
+    """accept_commit() into a token-major and/or paged cache (storage as for
+    verify_kv; the pages the appended rows fall in must be in block_table).
+    Returns (accepted, n_accepted, next_token)."""
+    if order not in ("hnd", "nhd"):
+        raise ValueError("order must be 'hnd' or 'nhd'")
+    nhd = order == "nhd"
+    _check(parents, "parents", torch.int32, 2)
+    dev = parents.device
+    for t, n in ((draft, "draft"), (target, "target")):
+        _check(t, n, torch.int32, 2, dev)
+    for t, n in ((k_spec, "k_spec"), (v_spec, "v_spec"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4, dev)
+    _check(cache_lens, "cache_lens", torch.int32, 1, dev)
+    B, T = parents.shape
+    if draft.shape != parents.shape or target.shape != parents.shape:
+        raise ValueError("parents, draft and target must share [B][T]")
+    rows, Hkv = (k_cache.shape[1], k_cache.shape[2]) if nhd else (k_cache.shape[2], k_cache.shape[1])
+    d = k_cache.shape[3]
+    want = (B, T, Hkv, d) if nhd else (B, Hkv, T, d)
+    if tuple(k_spec.shape) != want or v_spec.shape != k_spec.shape or v_cache.shape != k_cache.shape:
+        raise ValueError(f"k_spec/v_spec must be {want}, v_cache shaped as k_cache")
+    if tuple(cache_lens.shape) != (B,):
+        raise ValueError("cache_lens must be [B]")
+    lay = HtaKvLayout(KV_NHD if nhd else KV_HND, 0, 0, 0, None)
+    if block_table is None:
+        if k_cache.shape[0] != B:
+            raise ValueError("a contiguous cache has one block of Lmax rows per sequence")
+        Lmax = rows
+    else:
+        _check(block_table, "block_table", torch.int32, 2, dev)
+        if block_table.shape[0] != B:
+            raise ValueError("block_table must be [B][max_pages]")
+        lay.page_size, lay.max_pages, lay.num_pages = rows, block_table.shape[1], k_cache.shape[0]
+        lay.block_table = block_table.data_ptr()
+        Lmax = rows * block_table.shape[1]
+    dims = HtaDims(B, T, Hkv, Hkv, d, Lmax, 0.0)
+    if out is None:
+        accepted = torch.empty((B, T), dtype=torch.int32, device=dev)
+        n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
+        nxt = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        accepted, n_acc, nxt = out
+    if dev_err is not None:
+        _check(dev_err, "dev_err", torch.int32, 1, dev)
+    with torch.cuda.device(dev):
+        _raise(load().hta_accept_commit_kv(ctypes.byref(dims), ctypes.byref(lay), _ptr(parents), _ptr(draft),
+                                           _ptr(target), _ptr(k_spec), _ptr(v_spec), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(cache_lens), _ptr(accepted), _ptr(n_acc), _ptr(nxt),
+                                           _ptr(dev_err), _stream(dev)), "hta_accept_commit_kv")
     return accepted, n_acc, nxt
 
 

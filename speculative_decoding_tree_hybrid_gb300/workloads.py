@@ -241,6 +241,65 @@ def random_inputs(B: int, T: int, Hq: int, Hkv: int, d: int, lens, *, seed: int,
     return Inputs(cfg, q, kc, vc, lens, ks, vs, parents)
 
 
+# --------------------------------------------------------------------------- cache storage
+
+def kv_nhd(x: np.ndarray) -> np.ndarray:
+    """Head-major [outer][Hkv][rows][d] -> token-major [outer][rows][Hkv][d]."""
+    return np.ascontiguousarray(np.swapaxes(x, 1, 2))
+
+
+def paged_kv(k_cache: np.ndarray, v_cache: np.ndarray, lens, page_size: int, *, order: str = "hnd",
+             seed: int = 0, spare: int = 3, reserve: bool = False):
+    """Scatters contiguous caches [B][Hkv][Lmax][d] into a pool of pages.
+
+    Page i of sequence b (tokens i*P .. i*P + P - 1) goes to pool page
+    block_table[b][i]; the used pages of all sequences are spread over
+    n_used + spare pool pages by a seeded permutation. Rows past L_b in a
+    sequence's last page, and the pool pages no sequence uses, hold NaN;
+    table entries past a sequence's pages are -1; max_pages = ceil(Lmax / P).
+    order "nhd" stores each page token-major. reserve: every sequence gets
+    pages for all Lmax tokens (room to append rows). Returns (k_pool, v_pool,
+    block_table int32 [B][max_pages])."""
+    B, Hkv, Lmax, d = k_cache.shape
+    P = int(page_size)
+    lens = np.asarray(lens, dtype=np.int64).reshape(B)
+    max_pages = max(1, -(-Lmax // P))
+    used = [max_pages if reserve else -(-int(L) // P) for L in lens]
+    n_pool = sum(used) + spare
+    perm = np.random.default_rng(np.random.SeedSequence([5000, seed])).permutation(n_pool)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    kp = np.full((n_pool, Hkv, P, d), BF16_NAN, dtype=np.uint16)
+    vp = np.full_like(kp, BF16_NAN)
+    n = 0
+    for b in range(B):
+        for i in range(used[b]):
+            pg = int(perm[n])
+            n += 1
+            table[b, i] = pg
+            lo, hi = i * P, min((i + 1) * P, int(lens[b]))
+            if hi > lo:  # a reserved page past L_b stays NaN
+                kp[pg, :, :hi - lo] = k_cache[b, :, lo:hi]
+                vp[pg, :, :hi - lo] = v_cache[b, :, lo:hi]
+    if order == "nhd":
+        kp, vp = kv_nhd(kp), kv_nhd(vp)
+    return kp, vp, table
+
+
+def unpage_kv(pool: np.ndarray, table: np.ndarray, lens, Lmax: int, *, order: str = "hnd") -> np.ndarray:
+    """Inverse of paged_kv for one pool: contiguous [B][Hkv][Lmax][d], NaN past L_b."""
+    if order == "nhd":
+        pool = np.swapaxes(pool, 1, 2)
+    _, Hkv, P, d = pool.shape
+    B = table.shape[0]
+    out = np.full((B, Hkv, Lmax, d), BF16_NAN, dtype=np.uint16)
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(-(-L // P)):
+            lo, hi = i * P, min((i + 1) * P, L)
+            out[b, :, lo:hi] = pool[int(table[b, i]), :, :hi - lo]
+    return out
+
+
 # --------------------------------------------------------------------------- draft model
 
 @dataclasses.dataclass
