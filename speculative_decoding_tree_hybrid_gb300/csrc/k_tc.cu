@@ -110,12 +110,16 @@ __device__ void producer(const AttnParams &p, const TcMaps &maps, TcShared &sh, 
             const uint32_t full = bar_addr(sh.full[st]);
             mbar_arrive_expect_tx_if(leader, full, kTileBytes);
             if constexpr (!kGeneric) {
-                tma_load_3d_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, policy);
-                tma_load_3d_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z, policy);
+                // lanes 0 and 1 issue the two 64-dim halves in one instruction
+                const uint32_t h = threadIdx.x & 1;
+                tma_load_3d_hint((threadIdx.x & 31) < 2 ? 1u : 0u, ring + st * kTileBytes + h * kSubBytes, map, full,
+                                 (int)h * 64, y, z, policy);
             } else {
-                kv_tile_4d(p, pw, tree, t.b, t.kvh, y, t.Lb, [&](uint32_t off, int c0, int c1, int c2, int c3) {
-                    tma_load_4d_hint(leader, ring + st * kTileBytes + off, map, full, c0, c1, c2, c3, policy);
-                });
+                kv_tile_4d(p, pw, tree, t.b, t.kvh, y, t.Lb,
+                           [&](bool on, uint32_t off, int c0, int c1, int c2, int c3) {
+                               tma_load_4d_hint(on ? 1u : 0u, ring + st * kTileBytes + off, map, full, c0, c1, c2,
+                                                c3, policy);
+                           });
             }
         }
     }

@@ -148,14 +148,16 @@ __device__ void producer(const AttnParams &p, const Tc2Maps &maps, Tc2Shared &sh
         if ((uint32_t)is_v == rank) {
             const CUtensorMap *map = tree ? (is_v ? &maps.vs : &maps.ks) : (is_v ? &maps.vc : &maps.kc);
             if constexpr (!kGeneric) {
-                tma_load_3d_mc_hint(leader, ring + st * kTileBytes, map, full, 0, y, z, cluster_mask(p), policy);
-                tma_load_3d_mc_hint(leader, ring + st * kTileBytes + kSubBytes, map, full, 64, y, z,
-                                    cluster_mask(p), policy);
+                // lanes 0 and 1 issue the two 64-dim halves in one instruction
+                const uint32_t h = threadIdx.x & 1;
+                tma_load_3d_mc_hint((threadIdx.x & 31) < 2 ? 1u : 0u, ring + st * kTileBytes + h * kSubBytes, map,
+                                    full, (int)h * 64, y, z, cluster_mask(p), policy);
             } else {
-                kv_tile_4d(p, pw, tree, t.b, t.kvh, y, t.Lb, [&](uint32_t off, int c0, int c1, int c2, int c3) {
-                    tma_load_4d_mc_hint(leader, ring + st * kTileBytes + off, map, full, c0, c1, c2, c3,
-                                        cluster_mask(p), policy);
-                });
+                kv_tile_4d(p, pw, tree, t.b, t.kvh, y, t.Lb,
+                           [&](bool on, uint32_t off, int c0, int c1, int c2, int c3) {
+                               tma_load_4d_mc_hint(on ? 1u : 0u, ring + st * kTileBytes + off, map, full, c0, c1,
+                                                   c2, c3, cluster_mask(p), policy);
+                           });
             }
         }
         ++j;

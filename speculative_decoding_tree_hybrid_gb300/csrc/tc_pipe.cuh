@@ -106,12 +106,11 @@ __device__ __forceinline__ int32_t table_entry(const AttnParams &p, int32_t b, i
     return s < p.max_pages ? __ldg(p.block_table + (int64_t)b * p.max_pages + s) : 0;
 }
 
-// Pool page of cache token j of sequence b. Warp-collective: every lane
-// calls it with the same (b, j). An entry outside the pool is flagged and
-// read as page 0.
-__device__ __forceinline__ int32_t page_of(const AttnParams &p, PageWindow &w, int32_t b, int32_t j) {
-    const int32_t slot = j / p.page_size, lane = (int32_t)(threadIdx.x & 31);
-    if (b != w.b || slot < w.base || slot >= w.base + 64) {
+// Makes the window hold the entries of slots [slot, slot + n), n <= 32, of
+// sequence b. Warp-collective (same arguments in every lane).
+__device__ __forceinline__ void window_cover(const AttnParams &p, PageWindow &w, int32_t b, int32_t slot, int32_t n) {
+    const int32_t lane = (int32_t)(threadIdx.x & 31);
+    if (b != w.b || slot < w.base || slot + n > w.base + 64) {
         w.b = b;
         w.base = slot;
         w.entry = table_entry(p, b, slot + lane);
@@ -121,12 +120,14 @@ __device__ __forceinline__ int32_t page_of(const AttnParams &p, PageWindow &w, i
         w.entry = w.next;
         w.next = table_entry(p, b, w.base + 32 + lane);
     }
-    int32_t pg = __shfl_sync(0xffffffffu, w.entry, slot - w.base);
-    if (pg < 0 || pg >= p.num_pages) {
-        if (lane == 0) flag_error(p.dev_err, HTA_DEVERR_PAGE);
-        pg = 0;
-    }
-    return pg;
+}
+
+// Entry of slot s (inside the window) for this lane; every lane calls it.
+__device__ __forceinline__ int32_t window_entry(const PageWindow &w, int32_t s) {
+    const int32_t k = s - w.base;
+    const int32_t e0 = __shfl_sync(0xffffffffu, w.entry, k & 31);
+    const int32_t e1 = __shfl_sync(0xffffffffu, w.next, k & 31);
+    return k < 32 ? e0 : e1;
 }
 
 // Copies of one 128-key K or V tile whose first key is y (a cache token, or
@@ -134,33 +135,41 @@ __device__ __forceinline__ int32_t page_of(const AttnParams &p, PageWindow &w, i
 // through 4-D tensor maps: head-major (d, rows, Hkv, outer), token-major
 // (d, Hkv, rows, outer), outer = the sequence or the pool page. One box per
 // 64-dim half and per page the tile spans (boxes of min(page_size, 128)
-// rows); a box past the sequence's last page reads page 0 (those keys are
-// masked and their V rows cleared like any key past the end).
-// load4(shared-memory offset in the tile, c0, c1, c2, c3) issues one box.
+// rows, at most 16), each issued by its own lane in one warp instruction:
+// lane i copies half i % 2 of the rows from (i / 2) * rows. A box past the
+// sequence's last page reads page 0 (those keys are masked and their V rows
+// cleared like any key past the end); an entry outside the pool is flagged
+// and read as page 0.
+// load4(on, shared-memory offset in the tile, c0, c1, c2, c3): every lane
+// calls it; the lanes with `on` issue their box.
 template <typename Load4>
 __device__ __forceinline__ void kv_tile_4d(const AttnParams &p, PageWindow &w, bool tree, int32_t b, int32_t kvh,
                                            int32_t y, int32_t Lb, Load4 &&load4) {
     constexpr uint32_t kHalf = 128 * 64 * 2;  // one 64-dim half of a tile
+    const int32_t lane = (int32_t)(threadIdx.x & 31), h = lane & 1;
     if (tree || p.page_size == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (p.kv_nhd) load4(h * kHalf, h * 64, kvh, y, b);
-            else load4(h * kHalf, h * 64, y, kvh, b);
-        }
+        const bool on = lane < 2;
+        if (p.kv_nhd) load4(on, h * kHalf, h * 64, kvh, y, b);
+        else load4(on, h * kHalf, h * 64, y, kvh, b);
         return;
     }
-    const int32_t rows = p.page_size < 128 ? p.page_size : 128;
-    for (int32_t r = 0; r < 128; r += rows) {
-        const int32_t j = y + r;
-        const int32_t pg = j < Lb ? page_of(p, w, b, j) : 0;
-        const int32_t row = j % p.page_size;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t off = h * kHalf + (uint32_t)r * 128;
-            if (p.kv_nhd) load4(off, h * 64, kvh, row, pg);
-            else load4(off, h * 64, row, kvh, pg);
-        }
+    const int32_t P = p.page_size, rows = P < 128 ? P : 128;
+    const int32_t pages = 128 / rows;         // pages (or 128-row parts of one) in the tile
+    const bool on = lane < 2 * pages;
+    const int32_t r = on ? (lane >> 1) * rows : 0;
+    const int32_t j = y + r, slot0 = y / P;
+    window_cover(p, w, b, slot0, P < 128 ? pages : 1);
+    int32_t pg = window_entry(w, j / P);
+    if (!(on && j < Lb)) {
+        pg = 0;
+    } else if (pg < 0 || pg >= p.num_pages) {
+        flag_error(p.dev_err, HTA_DEVERR_PAGE);
+        pg = 0;
     }
+    const int32_t row = j % P;
+    const uint32_t off = h * kHalf + (uint32_t)r * 128;
+    if (p.kv_nhd) load4(on, off, h * 64, kvh, row, pg);
+    else load4(on, off, h * 64, row, kvh, pg);
 }
 
 }  // namespace tcp
