@@ -3,9 +3,35 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "hta_internal.cuh"
 
 namespace hta {
+
+// Launches `kern` with the n attributes in attrs[0 .. n) plus programmatic
+// stream serialization (attrs must have room for n + 1): the kernel may then
+// start while the kernel before it on the stream is still running, and waits
+// for it (griddep_wait) before reading any input. If the runtime rejects that
+// attribute with the others, the launch is repeated without it, and so are
+// all later launches of the process.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(cudaLaunchConfig_t cfg, cudaLaunchAttribute *attrs, int n, void (*kern)(KArgs...),
+                             Args &&...args) {
+    static std::atomic<int> allowed{1};
+    cfg.attrs = attrs;
+    if (allowed.load(std::memory_order_relaxed)) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = (unsigned)(n + 1);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+        if (e == cudaSuccess) return e;
+        (void)cudaGetLastError();
+        allowed.store(0, std::memory_order_relaxed);
+    }
+    cfg.numAttrs = (unsigned)n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // CUDA-core path (k_cc.cu)
 int cc_rows_per_group();

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(HTA_TMAX) k_build_mask(const int32_t *__restri
     __shared__ int bad_s;
     const int b = blockIdx.x, i = threadIdx.x;
     const int32_t *par = parents + (int64_t)b * T;
+    tc::griddep_launch_dependents();  // the attention launch may set up meanwhile
     if (i == 0) bad_s = 0;
     __syncthreads();
     int32_t pi = -1;

@@ -452,6 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before();
     }
+    // everything above reads no input: with a programmatic dependent launch
+    // it overlaps the kernel before this one on the stream
+    griddep_wait();
     build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
@@ -519,12 +522,10 @@ cudaError_t launch_stages(const AttnParams &p, const TcMaps &maps, int grid, cud
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_tc_verify<kStages, kGeneric>, p, maps);
+    return launch_dependent(cfg, attr, 1, k_tc_verify<kStages, kGeneric>, p, maps);
 }
 
 }  // namespace

@@ -545,6 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before();
     }
+    // everything above reads no input: with a programmatic dependent launch
+    // it overlaps the kernel before this one on the stream
+    griddep_wait();
     build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
     // every CTA's barriers exist before any multicasts into another
     cluster_sync_all();
@@ -603,16 +606,14 @@ cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cu
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = (unsigned)p.csize;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_tc2_verify<kStages, kGeneric>, p, maps);
+    return launch_dependent(cfg, attr, 2, k_tc2_verify<kStages, kGeneric>, p, maps);
 }
 
 template <int kStages>
