@@ -124,6 +124,10 @@ SMALL = [
     (1, 65, 16, 4, 128, [600], "uniform"),          # short last row group, odd nodes per group
     (1, 64, 64, 8, 128, [777], "window8_depth8"),   # G = 8: 512 rows, clusters of four CTAs
     (3, 64, 40, 8, 128, [300, 1029, 0], "window8_depth8"),  # QwQ shape, ragged incl. an empty cache
+    (1, 256, 32, 8, 128, [700], "window8_depth8"),  # largest tree: 1024 rows, two groups of four CTAs
+    (1, 256, 64, 8, 128, [300], "uniform"),         # largest tree at G = 8: 2048 rows, four row groups
+    # largest batch, ragged lengths 0 .. 299 (a few empty caches)
+    (1024, 4, 8, 2, 128, [int(x) for x in np.random.default_rng(3).integers(0, 300, 1024)], "uniform"),
 ]
 
 
