@@ -19,8 +19,11 @@
 // the ring into shared memory with bulk copies (two when the tile wraps past
 // the ring's end), into a ring of three stages so two tiles are in flight
 // while the current one is used. Warp w takes keys 8w .. 8w+7 of every tile: its lanes
-// split the head dimension (d/32 columns each), a dot product is a warp
-// reduction, and the same columns then accumulate P V with no exchange.
+// split the head dimension (d/32 columns each) for the 32 (key, row) dot
+// products, and one butterfly reduce-scatter (31 shuffles) leaves lane L the
+// full score of key L / 4 and row L % 4; the softmax of a row runs over its 8
+// lanes (one exponential per lane), and the probabilities go back to every
+// lane through shared memory for P V, accumulated on the same columns.
 // Each warp keeps an online softmax (base 2) per row; the 8 partial states
 // are merged in shared memory by the log-sum-exp rule at the end.
 #include "hta_internal.cuh"
@@ -37,9 +40,29 @@ constexpr int kTile = 64;              // keys per tile
 constexpr int kKeysPerWarp = kTile / kWarps;
 constexpr int kStages = 3;
 
-__device__ __forceinline__ float wsum(float v) {
+// One step of the reduce-scatter over v[0 .. 2n): the lane with bit n set
+// keeps the upper half, its partner the lower one, each adding the other's
+// copy; after the steps n = 16, 8, 4, 2, 1, v[0] of lane L is the sum over
+// all lanes of the input v[L].
+template <int n>
+__device__ __forceinline__ void scatter_step(float (&v)[32], int lane) {
+    const bool up = (lane & n) != 0;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int q = 0; q < n; ++q) {
+        const float lo = v[q], hi = v[q + n];
+        v[q] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, n);
+    }
+}
+
+// max / sum over the 8 lanes that share lane % 4
+__device__ __forceinline__ float row_max(float v) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
@@ -58,6 +81,7 @@ struct WinSmem {
         } ring;
         WinMerge<D> merge;  // reuses the idle ring after the last tile
     };
+    alignas(16) float prob[kWarps][32];  // a warp's probabilities of one tile, (key, row) pair L = 4 key + row
     uint64_t full[kStages];
     int32_t status;
 };
@@ -113,15 +137,12 @@ __global__ void __launch_bounds__(kThreads)
 
     // this lane's columns of the group's queries, scaled; padding rows are zero
     float q[kRows][CPL];
-    int64_t tq[kRows];  // query position of each row (-1: padding, sees nothing)
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
-        tq[i] = -1;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) q[i][c] = 0.f;
         if (i < nrows) {
             const int r = r_base + i, t = r / p.G, hq = kvh * p.G + (r - t * p.G);
-            tq[i] = P + t;
             const __nv_bfloat16 *qr = p.q + (((int64_t)b * p.T + t) * p.Hq + hq) * D + lane * CPL;
 #pragma unroll
             for (int c = 0; c < CPL; c += 2) {
@@ -131,14 +152,15 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
     }
-    float m[kRows], l[kRows], acc[kRows][CPL];
+    // running max and denominator of row lane % 4 (the 8 lanes of a row hold
+    // the same values); O of every row on this lane's columns
+    const int row_l = lane & 3, key_l = lane >> 2;
+    const int64_t tq_l = row_l < nrows ? P + (r_base + row_l) / p.G : -1;
+    float m_l = -INFINITY, l_l = 0.f, acc[kRows][CPL];
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-        m[i] = -INFINITY;
-        l[i] = 0.f;
+    for (int i = 0; i < kRows; ++i)
 #pragma unroll
         for (int c = 0; c < CPL; ++c) acc[i][c] = 0.f;
-    }
     __syncthreads();  // barriers initialised
 
     for (int it = 0; it < n_tiles; ++it) {
@@ -159,8 +181,8 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t j0 = j_begin + (int64_t)it * kTile;
         const int n = (int)min((int64_t)kTile, j_end - j0);
         const int k_lo = warp * kKeysPerWarp, k_hi = min(n, k_lo + kKeysPerWarp);
-        // scores of this warp's keys (lanes over the columns, then a warp sum)
-        float s[kRows][kKeysPerWarp];
+        // partial scores of this warp's (key, row) pairs on this lane's columns
+        float v[32];
 #pragma unroll
         for (int kk = 0; kk < kKeysPerWarp; ++kk) {
             const int key = k_lo + kk;
@@ -182,43 +204,40 @@ __global__ void __launch_bounds__(kThreads)
                 float d = 0.f;
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) d = fmaf(q[i][c], kf[c], d);
-                s[i][kk] = d;
+                v[kk * kRows + i] = d;
             }
         }
-#pragma unroll
-        for (int kk = 0; kk < kKeysPerWarp; ++kk)
-#pragma unroll
-            for (int i = 0; i < kRows; ++i) {
-                const int64_t j = j0 + k_lo + kk;
-                const float d = wsum(s[i][kk]);
-                // visibility: P + t - W < j <= P + t, and a key of this tile
-                s[i][kk] = (k_lo + kk < k_hi && j <= tq[i] && j > tq[i] - W) ? d : -INFINITY;
-            }
-        // online softmax per row over the warp's keys, then O += P V
+        scatter_step<16>(v, lane);
+        scatter_step<8>(v, lane);
+        scatter_step<4>(v, lane);
+        scatter_step<2>(v, lane);
+        scatter_step<1>(v, lane);
+        // lane L: key k_lo + L / 4, row L % 4; visible when P + t - W < j <= P + t
+        const int64_t j = j0 + k_lo + key_l;
+        const float s = (k_lo + key_l < k_hi && j <= tq_l && j > tq_l - W) ? v[0] : -INFINITY;
+        // online softmax of each row over its 8 lanes
+        const float m_new = fmaxf(m_l, row_max(s));
+        float alpha = 1.f, pr = 0.f;
+        if (m_new > -INFINITY) {
+            alpha = exp2f(m_l - m_new);  // 0 while the old max is -inf
+            pr = exp2f(s - m_new);       // 0 for an invisible key
+            m_l = m_new;
+        }
+        l_l = l_l * alpha + row_sum(pr);
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
-            float mx = -INFINITY;
+            const float a = __shfl_sync(0xffffffffu, alpha, i);  // lane i holds row i
 #pragma unroll
-            for (int kk = 0; kk < kKeysPerWarp; ++kk) mx = fmaxf(mx, s[i][kk]);
-            const float m_new = fmaxf(m[i], mx);
-            if (m_new > -INFINITY) {
-                const float alpha = exp2f(m[i] - m_new);  // 0 while the old max is -inf
-                l[i] *= alpha;
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[i][c] *= alpha;
-                m[i] = m_new;
-#pragma unroll
-                for (int kk = 0; kk < kKeysPerWarp; ++kk) {
-                    const float pk = exp2f(s[i][kk] - m_new);  // 0 for an invisible key
-                    s[i][kk] = pk;
-                    l[i] += pk;
-                }
-            }
+            for (int c = 0; c < CPL; ++c) acc[i][c] *= a;
         }
+        sm.prob[warp][lane] = pr;
+        __syncwarp();
+        // O += P V on this lane's columns
 #pragma unroll
         for (int kk = 0; kk < kKeysPerWarp; ++kk) {
             const int key = k_lo + kk;
             if (key >= k_hi) break;  // rows past the copied ones are stale
+            const float4 pk = *reinterpret_cast<const float4 *>(&sm.prob[warp][kk * kRows]);
             float vf[CPL];
 #pragma unroll
             for (int c = 0; c < CPL; c += 2) {
@@ -228,12 +247,14 @@ __global__ void __launch_bounds__(kThreads)
                 vf[c + 1] = x.y;
             }
 #pragma unroll
-            for (int i = 0; i < kRows; ++i)
-                if (m[i] > -INFINITY) {
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[i][c] = fmaf(s[i][kk], vf[c], acc[i][c]);
-                }
+            for (int c = 0; c < CPL; ++c) {
+                acc[0][c] = fmaf(pk.x, vf[c], acc[0][c]);
+                acc[1][c] = fmaf(pk.y, vf[c], acc[1][c]);
+                acc[2][c] = fmaf(pk.z, vf[c], acc[2][c]);
+                acc[3][c] = fmaf(pk.w, vf[c], acc[3][c]);
+            }
         }
+        __syncwarp();  // prob is rewritten by the next tile
         __syncthreads();  // stage it % kStages is free for tile it + kStages
     }
 
@@ -242,10 +263,10 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = 0; i < kRows; ++i) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) sm.merge.acc[warp][i][lane * CPL + c] = acc[i][c];
-        if (lane == 0) {
-            sm.merge.m[warp][i] = m[i];
-            sm.merge.l[warp][i] = l[i];
-        }
+    }
+    if (lane < kRows) {  // lane i holds row i
+        sm.merge.m[warp][lane] = m_l;
+        sm.merge.l[warp][lane] = l_l;
     }
     __syncthreads();
     const bool ok = sm.status != 0;
