@@ -545,12 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before();
     }
+    // every CTA's barriers exist before any multicasts into another: the
+    // cluster barrier's round trip overlaps the schedule below
+    cluster_arrive();
     // everything above reads no input: with a programmatic dependent launch
     // it overlaps the kernel before this one on the stream
     griddep_wait();
     build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
-    // every CTA's barriers exist before any multicasts into another
-    cluster_sync_all();
+    cluster_wait();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const int64_t u0 = lo_s[worker], u1 = lo_s[worker + 1];

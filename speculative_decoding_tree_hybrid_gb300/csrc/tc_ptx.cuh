@@ -304,6 +304,12 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
 }
 // every thread of every CTA of the cluster; orders shared-memory state
 // (barrier initialisation) before the peers use it
+// the two halves of cluster_sync_all, for CTA-local work in between
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
