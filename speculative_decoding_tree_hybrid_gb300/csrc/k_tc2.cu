@@ -577,11 +577,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    // the peer's last multicast fills and releases have reached this CTA
-    cluster_sync_all();
-    // Q and the K/V ring are idle now: they stage the merge
+    // Every multicast fill of this CTA's ring has landed (its own waits saw
+    // each tile), so Q and the ring are idle now and stage the merge; the
+    // peers' last releases may still arrive on this CTA's ring barriers,
+    // outside that region, so the CTA leaves only after every CTA of the
+    // cluster has come this far
+    cluster_arrive();
     merge_phase<128>(p, lens_s, pre_s, lo_s, smem + kOffQ, off_shared(kStages) - kOffQ);
     grid_barrier_depart(p);
+    cluster_wait();
 }
 
 size_t tc2_smem_bytes(int stages, int B, int workers) {
