@@ -98,3 +98,12 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kv_layout_option():
+    assert bench.parse_kv_layout("hnd") == ("hnd", 0)
+    assert bench.parse_kv_layout("nhd") == ("nhd", 0)
+    assert bench.parse_kv_layout("nhd:16") == ("nhd", 16)
+    assert bench.parse_kv_layout("hnd:256") == ("hnd", 256)
+    with pytest.raises(SystemExit):
+        bench.parse_kv_layout("bshd")
