@@ -95,3 +95,22 @@ def test_workspace_query_without_device_is_zero_or_sized(lib):
     n = hta.workspace_bytes(_dims())
     assert n == 0 or n >= 256
     assert hta.workspace_bytes(_dims(d=96)) == 0
+
+
+def test_binding_refuses_host_tensors():
+    """The binding has no CPU path: host tensors are rejected before any call."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((1, 8, 4, 64), dtype=torch.bfloat16)
+    kc = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16)
+    lens = torch.zeros(1, dtype=torch.int32)
+    ks = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    mask = torch.zeros((1, 8, 1), dtype=torch.int32)
+    parents = torch.zeros((1, 8), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        hta.verify(q, kc, kc, lens, ks, ks, mask)
+    with pytest.raises(ValueError, match="CUDA"):
+        hta.verify_kv(q, kc, kc, lens, ks, ks, mask, order="nhd")
+    with pytest.raises(ValueError, match="CUDA"):
+        hta.prefix_attn(q, kc, kc, lens)
+    with pytest.raises(ValueError, match="CUDA"):
+        hta.build_mask(parents)
