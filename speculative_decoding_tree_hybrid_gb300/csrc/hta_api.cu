@@ -6,6 +6,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <initializer_list>
+
 #include "hta_launch.h"
 
 using hta::AttnParams;
@@ -19,6 +21,13 @@ constexpr size_t kWsAlign = 256;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// int32 / fp32 arrays (NULL entries are optional arguments and pass)
+bool aligned4(std::initializer_list<const void *> ps) {
+    for (const void *p : ps)
+        if (((uintptr_t)p & 3u) != 0) return false;
+    return true;
+}
 
 int num_sms_current() {
     int dev = 0, sms = 0;
@@ -57,6 +66,7 @@ hta_status check_layout(const hta_dims *d, const hta_kv_layout *l) {
     // a 128-key tile covers whole pages, or lies inside one
     if (!(P == 16 || P == 32 || P == 64 || P % 128 == 0)) return HTA_ERR_INVALID_ARG;
     if (!l->block_table || l->max_pages <= 0 || l->num_pages <= 0) return HTA_ERR_INVALID_ARG;
+    if (!aligned4({l->block_table})) return HTA_ERR_ALIGN;
     if (d->Lmax > (int64_t)l->max_pages * P) return HTA_ERR_INVALID_ARG;
     return HTA_OK;
 }
@@ -274,6 +284,7 @@ int32_t hta_last_path(void) { return g_last_path; }
 hta_status hta_build_mask(const int32_t *parents, int32_t B, int32_t T, uint32_t *mask,
                           int32_t *dev_err, cudaStream_t stream) {
     if (!parents || !mask || B <= 0 || T <= 0) return HTA_ERR_INVALID_ARG;
+    if (!aligned4({parents, mask, dev_err})) return HTA_ERR_ALIGN;
     if (T > HTA_TMAX || B > HTA_BMAX) return HTA_ERR_UNSUPPORTED;
     if (hta::mask_launch(parents, B, T, mask, dev_err, stream) != cudaSuccess) return HTA_ERR_CUDA;
     return HTA_OK;
@@ -299,8 +310,11 @@ hta_status hta_accept_commit_kv(const hta_dims *d, const hta_kv_layout *layout, 
     if (d->B <= 0 || d->T <= 0 || d->Hkv <= 0 || d->d <= 0 || d->Lmax < 0) return HTA_ERR_INVALID_ARG;
     if (d->d != 64 && d->d != 128) return HTA_ERR_UNSUPPORTED;
     if (d->T > HTA_TMAX || d->B > HTA_BMAX || d->Lmax > (int64_t)0x7fffffff) return HTA_ERR_UNSUPPORTED;
-    if (check_layout(d, layout) != HTA_OK) return HTA_ERR_INVALID_ARG;
+    const hta_status ls = check_layout(d, layout);
+    if (ls != HTA_OK) return ls;
     if (!aligned16(k_spec) || !aligned16(v_spec) || !aligned16(k_cache) || !aligned16(v_cache))
+        return HTA_ERR_ALIGN;
+    if (!aligned4({parents, draft, target, cache_lens, accepted, n_accepted, next_token, dev_err}))
         return HTA_ERR_ALIGN;
     hta::KvStore st = {};
     if (layout) {
@@ -328,6 +342,7 @@ hta_status hta_window_attn(const hta_dims *d, int32_t window, const hta_bf16 *q,
     // the first query still reads window - 1 positions older than itself
     if ((int64_t)window + d->T - 1 > d->Lmax) return HTA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_ring) || !aligned16(v_ring) || !aligned16(o)) return HTA_ERR_ALIGN;
+    if (!aligned4({pos, lse, dev_err})) return HTA_ERR_ALIGN;
     Layout L = {};
     L.n_rg = 1;
     L.rows_pg = d->T * (d->Hq / d->Hkv);
@@ -353,6 +368,7 @@ hta_status hta_logitspec_tree(int32_t B, int32_t V, int64_t Lh_max, int32_t T, i
     if (k > HTA_LSPEC_KMAX || k + 1 > V || m < 2 || m > HTA_LSPEC_MMAX || T > HTA_TMAX || B > HTA_BMAX ||
         Lh_max > (int64_t)0x7fffffff)
         return HTA_ERR_UNSUPPORTED;
+    if (!aligned4({logits, hist, hist_len, parents, tokens, n_nodes, next_token, dev_err})) return HTA_ERR_ALIGN;
     hta::LspecParams p;
     memset(&p, 0, sizeof p);
     for (int r = 0; r <= k; ++r) {
@@ -401,6 +417,7 @@ hta_status hta_prefix_attn(const hta_dims *d, const hta_bf16 *q, const hta_bf16 
     if (s != HTA_OK) return s;
     if (!q || !k_cache || !v_cache || !cache_lens || !o_c || !lse_c) return HTA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_c)) return HTA_ERR_ALIGN;
+    if (!aligned4({cache_lens, lse_c, dev_err})) return HTA_ERR_ALIGN;
     return run_attention(d, q, k_cache, v_cache, cache_lens, nullptr, nullptr, nullptr, o_c, lse_c,
                          true, true, false, workspace, workspace_bytes, dev_err, stream);
 }
@@ -412,6 +429,7 @@ hta_status hta_tree_attn(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k
     if (s != HTA_OK) return s;
     if (!q || !k_spec || !v_spec || !mask || !o_s || !lse_s) return HTA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_spec) || !aligned16(v_spec) || !aligned16(o_s)) return HTA_ERR_ALIGN;
+    if (!aligned4({mask, lse_s})) return HTA_ERR_ALIGN;
     // the tree pass is a few MFLOP per head: it always takes the CUDA-core kernel
     hta_dims dd = *d;
     const int gmax = max_grid(kPathCC, &dd);
@@ -439,6 +457,7 @@ hta_status hta_merge(const hta_dims *d, const float *o_c, const float *lse_c, co
     if (s != HTA_OK) return s;
     if (!o_c || !lse_c || !o_s || !lse_s || !o || !lse) return HTA_ERR_INVALID_ARG;
     if (!aligned16(o_c) || !aligned16(o_s) || !aligned16(o)) return HTA_ERR_ALIGN;
+    if (!aligned4({lse_c, lse_s, lse})) return HTA_ERR_ALIGN;
     const int64_t rows = (int64_t)d->B * d->T * d->Hq;
     if (hta::merge2_launch(rows, d->d, o_c, lse_c, o_s, lse_s, (__nv_bfloat16 *)o, lse, stream) !=
         cudaSuccess)
@@ -458,6 +477,7 @@ hta_status hta_verify(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k_ca
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_spec) ||
         !aligned16(v_spec) || !aligned16(o))
         return HTA_ERR_ALIGN;
+    if (!aligned4({cache_lens, mask, lse, dev_err})) return HTA_ERR_ALIGN;
     return run_attention(d, q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, o, lse, false,
                          true, true, workspace, workspace_bytes, dev_err, stream);
 }
@@ -475,6 +495,7 @@ hta_status hta_verify_kv(const hta_dims *d, const hta_kv_layout *layout, const h
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_spec) ||
         !aligned16(v_spec) || !aligned16(o))
         return HTA_ERR_ALIGN;
+    if (!aligned4({cache_lens, mask, lse, dev_err})) return HTA_ERR_ALIGN;
     return run_attention(d, q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, o, lse, false,
                          true, true, workspace, workspace_bytes, dev_err, stream, layout);
 }
@@ -488,6 +509,7 @@ hta_status hta_prefix_attn_kv(const hta_dims *d, const hta_kv_layout *layout, co
     if ((s = check_layout(d, layout)) != HTA_OK) return s;
     if (!q || !k_cache || !v_cache || !cache_lens || !o_c || !lse_c) return HTA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_c)) return HTA_ERR_ALIGN;
+    if (!aligned4({cache_lens, lse_c, dev_err})) return HTA_ERR_ALIGN;
     return run_attention(d, q, k_cache, v_cache, cache_lens, nullptr, nullptr, nullptr, o_c, lse_c,
                          true, true, false, workspace, workspace_bytes, dev_err, stream, layout);
 }

@@ -114,3 +114,22 @@ def test_binding_refuses_host_tensors():
         hta.prefix_attn(q, kc, kc, lens)
     with pytest.raises(ValueError, match="CUDA"):
         hta.build_mask(parents)
+
+
+def test_int32_arrays_must_be_4_byte_aligned(lib):
+    """A misaligned int32 / fp32 array is refused on the host (the device
+    would fault on it)."""
+    d = _dims()
+    good = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    # hta_verify: q, kc, vc, cache_lens, ks, vs, mask, o, lse, ws
+    for idx in (3, 6, 8):  # cache_lens, mask, lse
+        a = [good] * 10
+        a[idx] = odd
+        assert lib.hta_verify(ctypes.byref(d), *a, 1 << 20, None, None) == -3
+    # dev_err
+    assert lib.hta_verify(ctypes.byref(d), *([good] * 10), 1 << 20, odd, None) == -3
+    assert lib.hta_build_mask(odd, 1, 8, good, None, None) == -3
+    assert lib.hta_build_mask(good, 1, 8, odd, None, None) == -3
+    # hta_merge: o_c, lse_c, o_s, lse_s, o, lse
+    assert lib.hta_merge(ctypes.byref(d), good, odd, good, good, good, good, None) == -3

@@ -98,3 +98,8 @@ def test_paged_kv_reserve_maps_every_page():
     # pages past L_b are NaN: nothing was written into them
     assert np.all(kp[table[0, 2:]] == wl.BF16_NAN) and np.all(kp[table[1]] == wl.BF16_NAN)
     assert np.all(kp[table[0, 1], :, 36:] == wl.BF16_NAN)
+
+
+def test_misaligned_block_table_rejected(lib):
+    lay = hta.HtaKvLayout(0, 16, 16, 4, (1 << 20) + 2)
+    assert _call(lib, lay) == (-3, -3)
