@@ -12,8 +12,8 @@ L2, so each step reads its cache from HBM. Steps are replayed from a CUDA
 graph (one graph holds one step per cache), so host launch cost stays out of
 the device-timed loop.
 
-Output: one JSON line (rank 0). `value` is KV-cache GB/s over the whole job
-(all ranks); `us_per_layer_call` the mean hta_verify duration from CUDA events
+Output: one JSON line. `value` is KV-cache GB/s over the timed steps;
+`us_per_layer_call` the median hta_verify duration from CUDA events
 on the launching stream; `roofline` compares that kernel with the measured HBM
 copy bandwidth; `e2e` repeats the measurement through the public API with the
 inputs in pinned host memory (copies inside the timed region); `cpu_baseline`
@@ -21,8 +21,13 @@ times the fp64 CPU oracle on a bounded sample.
 
 --impl reference times the CPU oracle alone on the host cores (the reference
 arm: there is no runnable reference implementation of this method).
-With torchrun (WORLD_SIZE > 1) every rank runs an independent replica on its
-own GPU: the path shards by sequence and KV head with no exchange.
+
+The library runs on one GPU: its clustered kernel multicasts K/V tiles within
+a CTA cluster, and that code is only ever run in single-GPU processes. A run
+with more than one GPU (--gpus N > 1, or WORLD_SIZE > 1 under torchrun)
+therefore does no GPU work: rank 0 prints one JSON line with a "skipped"
+reason and every rank exits 0. The reference arm (CPU only) still runs on
+rank 0.
 """
 from __future__ import annotations
 
@@ -166,47 +171,44 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# --------------------------------------------------------------------------- distributed
+# --------------------------------------------------------------------------- process layout
 
-def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    pg = None
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-        pg = dist
-    return world, rank, local, pg
+def launch_env():
+    """(world size, rank) from the torchrun environment (1, 0 when absent)."""
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
 
 
-def reduce_max(pg, value: float, device=None) -> float:
-    if pg is None:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    return float(t.item())
+MULTI_GPU_SKIP = ("single-GPU library: its clustered kernel multicasts K/V tiles inside a CTA cluster "
+                  "and is run only in one-GPU processes, so no multi-GPU replicas are launched")
 
 
-def barrier(pg, device=None):
-    if pg is None:
-        return
-    if device is not None and device.type == "cuda":
-        pg.barrier(device_ids=[device.index])
-    else:
-        pg.barrier()
+def skipped_line(n_gpus: int) -> dict:
+    return {"metric": METRIC, "value": None, "unit": "GB/s", "n_gpus": n_gpus, "higher_is_better": True,
+            "scaling": "weak", "skipped": MULTI_GPU_SKIP}
 
 
-def aggregate(units_per_rank: float, elapsed_s: float, pg, device=None):
-    """Whole-job throughput: units of all ranks over the slowest rank's time."""
-    world = 1 if pg is None else pg.get_world_size()
-    t = reduce_max(pg, elapsed_s, device)
-    return units_per_rank * world / t, t
+def throughput(units: float, elapsed_s: float):
+    """Units per second over the timed region."""
+    return units / elapsed_s, elapsed_s
+
+
+def cpu_model() -> str:
+    """Host CPU model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 # --------------------------------------------------------------------------- CPU oracle
@@ -236,7 +238,7 @@ def oracle_sample(inp, rows_target: int, seconds: float):
     return per_call, oracle.num_threads(), desc, t_used, done_rows
 
 
-def run_reference(args, world, rank, pg):
+def run_reference(args, world, rank):
     if rank != 0:
         return
     cfg = wl.CONFIGS[args.config]
@@ -260,7 +262,7 @@ def run_reference(args, world, rank, pg):
               f"value extrapolates to the full layer-call")
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3),
         "us_per_layer_call": round(per_call * 1e6, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -284,14 +286,14 @@ def parse_kv_layout(text: str):
     return order, int(page) if page else 0
 
 
-def run_gpu(args, world, rank, local, pg):
+def run_gpu(args):
     import torch
 
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_tree_hybrid_gb300 import hta
 
-    dev = torch.device(f"cuda:{local}")
+    dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     cfg = wl.CONFIGS[args.config]
     n_sets = args.kv_sets
@@ -344,8 +346,10 @@ def run_gpu(args, world, rank, local, pg):
         hta.build_mask(parents, dev_err=err, out=mask)
         verify_call(k)
 
-    # one graph replays one step per K/V set
-    graph = None
+    # graphs: one of n_sets steps (one per K/V set) for the bulk of the steps,
+    # and one single-step graph per set for a remainder, so that a run of n
+    # steps replays exactly n steps with few host-side replays
+    multi, singles = None, None
     with torch.cuda.stream(stream):
         for _ in range(2):
             for k in range(n_sets):
@@ -358,31 +362,73 @@ def run_gpu(args, world, rank, local, pg):
                 with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
                     for k in range(n_sets):
                         one_step(k)
-                graph = g
+                gs = []
+                for k in range(n_sets):
+                    gk = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gk, stream=stream, capture_error_mode="thread_local"):
+                        one_step(k)
+                    gs.append(gk)
+                multi, singles = g, gs
             except Exception as e:  # capture unsupported: time eager launches instead
                 print(f"graph capture failed ({e}); timing eager launches", file=sys.stderr)
-                graph = None
+                multi, singles = None, None
                 torch.cuda.synchronize(dev)
 
     def run_steps(n):
         with torch.cuda.stream(stream):
+            if multi is None:
+                for i in range(n):
+                    one_step(i % n_sets)
+                return
             for _ in range(n // n_sets):
-                if graph is not None:
-                    graph.replay()
-                else:
-                    for k in range(n_sets):
-                        one_step(k)
+                multi.replay()
+            for k in range(n % n_sets):
+                singles[k].replay()
 
-    # warm-up
-    run_steps(max(args.warmup, 3) * n_sets)
+    warmup = max(args.warmup, 3)
+    steps = max(args.steps, 1)
+    run_steps(warmup)
     torch.cuda.synchronize(dev)
-    steps = (args.steps + n_sets - 1) // n_sets * n_sets
 
-    # per-launch hta_verify duration (CUDA events on the launching stream).
-    # A 512 MB memset ahead of each launch flushes L2 and keeps the stream
-    # busy while the events and the kernel are enqueued.
+    # hta_verify's average launch duration: a CUDA graph of verify launches
+    # only, back to back over the K/V sets (each set was evicted from L2 by the
+    # others since its last use), timed with CUDA events on the launching
+    # stream over `vreps` replays.
+    vgraph = None
+    if not args.no_graph:
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for k in range(n_sets):
+                    verify_call(k)
+            vgraph = g
+    vreps = max(8, args.launch_samples // n_sets)
+
+    def verify_round():
+        if vgraph is not None:
+            vgraph.replay()
+        else:
+            for k in range(n_sets):
+                verify_call(k)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            verify_round()
+        torch.cuda.synchronize(dev)
+        va, vb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        va.record(stream)
+        for _ in range(vreps):
+            verify_round()
+        vb.record(stream)
+    torch.cuda.synchronize(dev)
+    us_call = va.elapsed_time(vb) * 1e3 / (vreps * n_sets)
+
+    # isolated launches for reference: a 512 MB memset ahead of each launch
+    # flushes L2 and keeps the stream busy while the events and the kernel are
+    # enqueued; these durations also hold the events' own cost (a kernel that
+    # returns at once measures about 4-6 us this way)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    n_meas = max(4, min(args.launch_samples, steps))
+    n_meas = max(4, args.launch_samples)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_meas)]
     with torch.cuda.stream(stream):
@@ -395,54 +441,53 @@ def run_gpu(args, world, rank, local, pg):
             ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    us_call = statistics.median(per_launch_ms) * 1e3
+    us_isolated = statistics.median(per_launch_ms) * 1e3
     del flush
 
-    # timed region
+    # timed region: exactly `steps` steps
     err.zero_()
-    barrier(pg, dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with ClockSampler(0) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         run_steps(steps)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
-    barrier(pg, dev)
     elapsed = t_start.elapsed_time(t_end) / 1e3
     dev_err = int(err.item())
     if dev_err:
         raise SystemExit(f"device error flags {dev_err}")
 
     bytes_step = kv_bytes(base)
-    gbs, t_max = aggregate(bytes_step * steps / 1e9, elapsed, pg, dev)
+    gbs, t_el = throughput(bytes_step * steps / 1e9, elapsed)
 
     # end to end through the public API with host buffers (contiguous layout)
-    e2e = run_e2e(args, hta, sets, dev, pg) if default_layout else None
+    e2e = run_e2e(args, hta, sets, dev) if default_layout else None
 
-    if rank != 0:
-        return
     peak, peak_kind = measured_peak()
     achieved = bytes_step / (us_call * 1e-6) / 1e9
     kernel = {hta.PATH_TC: "k_tc_verify", hta.PATH_TC2: "k_tc2_verify"}.get(path, "k_cc_attn")
     traffic = recorded_traffic(cfg.name, kernel)
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline:
         per_call, cores, desc, _, _ = oracle_sample(base, args.cpu_rows, args.cpu_seconds)
         cpu = {"value": round(bytes_step / per_call / 1e9, 4), "unit": "GB/s", "cores": cores,
-               "kind": "oracle", "sample": desc}
+               "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),
         "unit": "GB/s",
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": steps,
-        "warmup": max(args.warmup, 3) * n_sets,
-        "ms_per_step": round(t_max / steps * 1e3, 5),
+        "warmup": warmup,
+        "ms_per_step": round(t_el / steps * 1e3, 5),
         "us_per_layer_call": round(us_call, 3),
-        "us_per_layer_call_p10_p90": [round(float(np.percentile(per_launch_ms, 10)) * 1e3, 3),
-                                      round(float(np.percentile(per_launch_ms, 90)) * 1e3, 3)],
+        "us_per_layer_call_timing": f"CUDA events over {vreps} replays of a graph of {n_sets} back-to-back "
+                                    f"hta_verify launches (one per K/V set)",
+        "us_per_isolated_launch": round(us_isolated, 3),
+        "us_per_isolated_launch_p10_p90": [round(float(np.percentile(per_launch_ms, 10)) * 1e3, 3),
+                                           round(float(np.percentile(per_launch_ms, 90)) * 1e3, 3)],
         "pct_hbm_roofline": round(100.0 * achieved / peak, 2),
         "higher_is_better": True,
         "scaling": "weak",
@@ -452,7 +497,8 @@ def run_gpu(args, world, rank, local, pg):
         "config": {"workload": workload_desc(cfg), "kv_sets": n_sets,
                    "kv_layout": ("contiguous " if not page else f"{page}-token pages, ") + order,
                    "l2": f"{n_sets} K/V caches of {bytes_step / 1e6:.1f} MB rotated (> 129 MB L2)",
-                   "graph": graph is not None, "path": {hta.PATH_TC: "tcgen05", hta.PATH_TC2: "tcgen05 CTA clusters"}.get(path, "cuda-core"),
+                   "graph": multi is not None,
+                   "path": {hta.PATH_TC: "tcgen05", hta.PATH_TC2: "tcgen05 CTA clusters"}.get(path, "cuda-core"),
                    "all_bytes_per_call": all_bytes(base)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -466,7 +512,7 @@ def run_gpu(args, world, rank, local, pg):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, hta, sets, dev, pg):
+def run_e2e(args, hta, sets, dev):
     """Same metric through the public API, inputs in pinned host memory: every
     step copies its inputs host->device, runs mask + verify, and reads o and
     lse back."""
@@ -509,7 +555,6 @@ def run_e2e(args, hta, sets, dev, pg):
         for k in range(3):
             one(k)
         torch.cuda.synchronize(dev)
-        barrier(pg, dev)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
@@ -517,9 +562,8 @@ def run_e2e(args, hta, sets, dev, pg):
             one(k)
         t1.record(stream)
         torch.cuda.synchronize(dev)
-    barrier(pg, dev)
     el = t0.elapsed_time(t1) / 1e3
-    gbs, t_max = aggregate(kv_bytes(base) * steps / 1e9, el, pg, dev)
+    gbs, t_max = throughput(kv_bytes(base) * steps / 1e9, el)
     return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": round(t_max / steps * 1e3, 4)}
@@ -540,7 +584,7 @@ def accept_inputs(B: int, T: int, seed: int):
     return parents, draft, target
 
 
-def run_accept(args, world, rank, local, pg):
+def run_accept(args):
     """The step after verification: accept walk + K/V append, timed alone on
     the ragged B = 32 shape (one layer's K/V).
 
@@ -554,7 +598,7 @@ def run_accept(args, world, rank, local, pg):
     __graft_entry__.build()
     from speculative_decoding_tree_hybrid_gb300 import hta
 
-    dev = torch.device(f"cuda:{local}")
+    dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     cfg = wl.CONFIGS["ragged_b32"]
     B, T, Hkv, d = cfg.B, cfg.T, cfg.Hkv, cfg.d
@@ -602,13 +646,11 @@ def run_accept(args, world, rank, local, pg):
     times = [a.elapsed_time(b) * 1e3 / k_graph for a, b in ev]
     us = statistics.median(times)
     moved = n_acc * Hkv * d * 2 * 2 * 2  # the accepted K and V rows, read once and written once
-    if rank != 0:
-        return
     peak, peak_kind = measured_peak()
     gbs = moved / (us * 1e-6) / 1e9
     print(json.dumps({
         "metric": "accept walk + K/V append, us per call", "op": "accept", "value": round(us, 3), "unit": "us",
-        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": world,
+        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": 1,
         "us_p10_p90": [round(float(np.percentile(times, 10)), 3), round(float(np.percentile(times, 90)), 3)],
         "timing": f"device time per call: CUDA graph of {k_graph} calls per timed replay",
         "config": {"workload": f"ragged_b32 shape: B={B} T={T} Hkv={Hkv} d={d}, window-8 depth<=8 trees, "
@@ -619,7 +661,7 @@ def run_accept(args, world, rank, local, pg):
         "gpu_launches": steps * k_graph, "dtype": "bf16", "data": "synthetic"}), flush=True)
 
 
-def run_drafter(args, world, rank, local, pg):
+def run_drafter(args):
     """The draft model's two attention kinds, timed alone through CUDA-graph
     replays (device time per call):
       cross:  prefix-only attention of one draft query per sequence over the
@@ -634,7 +676,7 @@ def run_drafter(args, world, rank, local, pg):
     __graft_entry__.build()
     from speculative_decoding_tree_hybrid_gb300 import hta
 
-    dev = torch.device(f"cuda:{local}")
+    dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     warmup, steps = max(args.warmup, 3), min(max(args.steps, 1), 200)
     Hq, Hkv, d = 32, 8, 128
@@ -688,13 +730,11 @@ def run_drafter(args, world, rank, local, pg):
     torch.cuda.synchronize(dev)
     times = [a.elapsed_time(b) * 1e3 / per_replay for a, b in ev]
     us = statistics.median(times)
-    if rank != 0:
-        return
     peak, peak_kind = measured_peak()
     gbs = moved / (us * 1e-6) / 1e9
     print(json.dumps({
         "metric": f"drafter {args.op} attention, us per call", "op": args.op, "value": round(us, 3), "unit": "us",
-        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": world,
+        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": 1,
         "us_p10_p90": [round(float(np.percentile(times, 10)), 3), round(float(np.percentile(times, 90)), 3)],
         "timing": f"device time per call: CUDA graph of {per_replay} calls per timed replay",
         "config": {"workload": workload},
@@ -704,7 +744,7 @@ def run_drafter(args, world, rank, local, pg):
         flush=True)
 
 
-def run_lspec(args, world, rank, local, pg):
+def run_lspec(args):
     """The LogitSpec draft-tree builder, timed alone through CUDA-graph
     replays: B = 32 sequences, LLaMA-3 vocabulary (128256 logits), 32K-token
     histories with copy structure, logits that favour tokens of the context
@@ -717,7 +757,7 @@ def run_lspec(args, world, rank, local, pg):
     __graft_entry__.build()
     from speculative_decoding_tree_hybrid_gb300 import hta
 
-    dev = torch.device(f"cuda:{local}")
+    dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     warmup, steps = max(args.warmup, 3), min(max(args.steps, 1), 200)
     B, V, Lh, k, m, T = 32, 128256, 32768, 60, 3, 64
@@ -750,14 +790,12 @@ def run_lspec(args, world, rank, local, pg):
     times = [a.elapsed_time(b) * 1e3 / per_replay for a, b in ev]
     us = statistics.median(times)
     nodes = int(out[2].sum().item())
-    if rank != 0:
-        return
     moved = B * V * 4 + B * Lh * 4 + 2 * B * T * 4  # logits and history read once, the trees written
     peak, peak_kind = measured_peak()
     gbs = moved / (us * 1e-6) / 1e9
     print(json.dumps({
         "metric": "LogitSpec draft-tree build, us per call", "op": "lspec", "value": round(us, 3), "unit": "us",
-        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": world,
+        "higher_is_better": False, "steps": steps, "warmup": warmup, "n_gpus": 1,
         "us_p10_p90": [round(float(np.percentile(times, 10)), 3), round(float(np.percentile(times, 90)), 3)],
         "timing": f"device time per call: CUDA graph of {per_replay} calls per timed replay",
         "config": {"workload": f"B={B} V={V} history {Lh} tokens (copy spans over a 4000-token vocabulary), "
@@ -792,21 +830,23 @@ def main(argv=None):
                          "cross / window: the draft model's cross-attention / sliding-window attention; "
                          "lspec: the LogitSpec draft-tree builder")
     args = ap.parse_args(argv)
-    world, rank, local, pg = dist_setup()
-    try:
-        if args.impl == "reference":
-            run_reference(args, world, rank, pg)
-        elif args.op == "accept":
-            run_accept(args, world, rank, local, pg)
-        elif args.op in ("cross", "window"):
-            run_drafter(args, world, rank, local, pg)
-        elif args.op == "lspec":
-            run_lspec(args, world, rank, local, pg)
-        else:
-            run_gpu(args, world, rank, local, pg)
-    finally:
-        if pg is not None:
-            pg.destroy_process_group()
+    world, rank = launch_env()
+    n_gpus = max(world, args.gpus)
+    if args.impl == "reference":
+        run_reference(args, n_gpus, rank)  # CPU only: rank 0 runs it, the others exit
+        return
+    if n_gpus > 1:
+        if rank == 0:
+            print(json.dumps(skipped_line(n_gpus)), flush=True)
+        return
+    if args.op == "accept":
+        run_accept(args)
+    elif args.op in ("cross", "window"):
+        run_drafter(args)
+    elif args.op == "lspec":
+        run_lspec(args)
+    else:
+        run_gpu(args)
 
 
 if __name__ == "__main__":

@@ -29,6 +29,25 @@ bool aligned4(std::initializer_list<const void *> ps) {
     return true;
 }
 
+// Memory of the current device (NULL passes: optional arguments). The
+// tensor-core kernels read their inputs through TMA tensor maps, and the
+// clustered one multicasts each tile to the CTAs of a cluster; those maps
+// must cover this GPU's own memory only.
+bool on_current_device(std::initializer_list<const void *> ps) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    for (const void *ptr : ps) {
+        if (!ptr) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        if (at.type != cudaMemoryTypeDevice || at.device != dev) return false;
+    }
+    return true;
+}
+
 int num_sms_current() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -173,6 +192,19 @@ int max_grid(int path, const hta_dims *d) {
     return path == kPathTC ? hta::tc_max_grid(d->B, sms) : hta::cc_max_grid(d->d, d->B, sms);
 }
 
+// Bound of the grid-barrier wait before the merge: ~4 s of SM cycles, or
+// HTA_TEST_BARRIER_WAIT_CYCLES (read on every call) for failure-detection
+// tests that make that wait run out on purpose.
+uint64_t barrier_wait_cycles() {
+    const char *s = getenv("HTA_TEST_BARRIER_WAIT_CYCLES");
+    if (s && *s) {
+        char *end = nullptr;
+        const unsigned long long v = strtoull(s, &end, 10);
+        if (end && *end == 0) return (uint64_t)v;
+    }
+    return 8000000000ull;
+}
+
 AttnParams base_params(const hta_dims *d, const Layout &L) {
     AttnParams p;
     memset(&p, 0, sizeof p);
@@ -192,6 +224,7 @@ AttnParams base_params(const hta_dims *d, const Layout &L) {
     p.tile = L.tile;
     p.n_tree_tiles = L.n_tree_tiles;
     p.subs = L.subs > 0 ? L.subs : 1;
+    p.bar_wait_cycles = barrier_wait_cycles();
     return p;
 }
 
@@ -201,6 +234,7 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
                          void *out_o, float *out_lse, bool out_fp32, bool use_cache, bool use_tree,
                          void *ws, size_t ws_bytes, int32_t *dev_err, cudaStream_t stream,
                          const hta_kv_layout *kvl = nullptr) {
+    if (!on_current_device({q, kc, vc, ks, vs})) return HTA_ERR_INVALID_ARG;
     const int path = choose_path(d);
     if (path == kPathNone) return HTA_ERR_UNSUPPORTED;
     const int gmax = max_grid(path, d);
@@ -393,7 +427,7 @@ hta_status hta_logitspec_tree(int32_t B, int32_t V, int64_t Lh_max, int32_t T, i
     return HTA_OK;
 }
 
-size_t hta_workspace_bytes(const hta_dims *d) {
+size_t hta_verify_workspace_bytes(const hta_dims *d, const int32_t *host_cache_lens) {
     if (check_dims(d) != HTA_OK) return 0;
     size_t best = 0;
     const int paths[3] = {kPathCC, kPathTC, kPathTC2};
@@ -401,13 +435,33 @@ size_t hta_workspace_bytes(const hta_dims *d) {
     for (int i = 0; i < 3; ++i) {
         if (paths[i] == kPathTC && !tc_ok) continue;
         if (paths[i] == kPathTC2 && !(tc_ok && tc2_fits(d))) continue;
-        const int g = max_grid(paths[i], d);
+        int g = max_grid(paths[i], d);
         if (g <= 0) continue;
+        if (host_cache_lens) {
+            // a grid no larger than the units these lengths make (as the call does)
+            const Layout L0 = make_layout(d, paths[i], 0, true);
+            int64_t tiles = 0;
+            for (int b = 0; b < d->B; ++b) {
+                int64_t L = host_cache_lens[b];
+                L = L < 0 ? 0 : (L > d->Lmax ? d->Lmax : L);
+                tiles += L0.n_tree_tiles + (L + L0.tile - 1) / L0.tile;
+            }
+            const int64_t units = tiles * d->Hkv * L0.n_rg;
+            if (paths[i] == kPathTC2) {
+                const int c = tc2_csize(d);
+                const int64_t w = units < (int64_t)(g / c) ? (units > 0 ? units : 1) : g / c;
+                g = (int)(w * c);
+            } else if (units < (int64_t)g) {
+                g = (int)(units > 0 ? units : 1);
+            }
+        }
         const Layout L = make_layout(d, paths[i], g, true);
         if (L.total > best) best = L.total;
     }
     return best;
 }
+
+size_t hta_workspace_bytes(const hta_dims *d) { return hta_verify_workspace_bytes(d, nullptr); }
 
 hta_status hta_prefix_attn(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k_cache,
                            const hta_bf16 *v_cache, const int32_t *cache_lens, float *o_c,
@@ -430,6 +484,7 @@ hta_status hta_tree_attn(const hta_dims *d, const hta_bf16 *q, const hta_bf16 *k
     if (!q || !k_spec || !v_spec || !mask || !o_s || !lse_s) return HTA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_spec) || !aligned16(v_spec) || !aligned16(o_s)) return HTA_ERR_ALIGN;
     if (!aligned4({mask, lse_s})) return HTA_ERR_ALIGN;
+    if (!on_current_device({q, k_spec, v_spec})) return HTA_ERR_INVALID_ARG;
     // the tree pass is a few MFLOP per head: it always takes the CUDA-core kernel
     hta_dims dd = *d;
     const int gmax = max_grid(kPathCC, &dd);

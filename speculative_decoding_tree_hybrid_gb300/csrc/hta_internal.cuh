@@ -76,6 +76,8 @@ struct AttnParams {
     // [B][max_pages]. kv_generic: anything but contiguous head-major.
     int32_t kv_nhd, page_size, max_pages, num_pages, kv_generic;
     const int32_t *block_table;
+    // bound of the grid-barrier wait before the merge, in SM cycles
+    uint64_t bar_wait_cycles;
 };
 
 // ---------------------------------------------------------------- errors
@@ -257,8 +259,11 @@ __device__ __forceinline__ int32_t rows_in_group(const AttnParams &p, int32_t rg
 
 // Grid-wide barrier for a cooperative launch (every CTA is resident), split
 // in two so that a CTA can do independent work between its arrival and the
-// wait. The wait is bounded by ~2 s of device time; on expiry the error flag
-// is set and the barrier reports failure instead of hanging.
+// wait. The wait is bounded (p.bar_wait_cycles, ~4 s of device time unless a
+// test sets a shorter bound); on expiry the error flag is set and the barrier
+// reports failure instead of hanging. Every async copy of the CTA has
+// completed before it waits here, so a CTA that gives up leaves nothing in
+// flight.
 // grid_barrier_depart returns the two counters to zero once the last CTA has
 // left.
 __device__ inline void grid_barrier_arrive(const AttnParams &p) {
@@ -278,7 +283,7 @@ __device__ inline bool grid_barrier_wait(const AttnParams &p) {
         for (;;) {
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.bar) : "memory");
             if (v >= gridDim.x) break;
-            if (cycles_now() - t0 > 2 * kWaitLimitCycles) {
+            if (cycles_now() - t0 > p.bar_wait_cycles) {
                 ok = 0;
                 flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
                 break;
@@ -338,7 +343,7 @@ constexpr uint32_t kMergePlanBytes = 6 * kMergeRuns * 4 + 16;  // run table, cop
 
 template <int D>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
-                                   const int64_t *lo_s, uint8_t *buf, uint32_t buf_bytes) {
+                                   const int64_t *lo_s, uint8_t *buf, uint32_t buf_bytes, bool arrived = false) {
     constexpr int HPL = D / 16;                 // columns per lane of a half-warp
     constexpr int REC = D + 4;                  // floats per record: O | m | l | w | pad
     constexpr uint32_t REC_BYTES = REC * 4;
@@ -374,7 +379,8 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
         tc::mbar_fence_init();
     }
 
-    grid_barrier_arrive(p);
+    if (!arrived) grid_barrier_arrive(p);
+    else __syncthreads();
     bool ok = true, waited = false;
     const uint32_t seg_lo = r0 / rows_pg, seg_end = r1 > r0 ? (r1 - 1) / rows_pg + 1 : seg_lo;
     for (uint32_t sb = seg_lo; sb < seg_end || !waited; sb += kMergeRuns) {

@@ -81,6 +81,7 @@ struct Tc2Shared {
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
+    int32_t arrived;  // the softmax warps have arrived on the grid barrier for this CTA
 };
 static_assert(sizeof(Tc2Shared) <= kSharedBytes, "shared control block too large");
 
@@ -316,6 +317,7 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         int64_t slot;
         float m, l;
     } pend = {false, false, 0, 0, 0, 0, 0, 0.f, 0.f};
+    int pend_rows = 0;
     bool ok = true;
     auto write_record = [&](int chunks) -> bool {
         if (pend.k == 0) {
@@ -482,16 +484,51 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         if (t.last) {
             if (pend.on && !write_record(4)) break;  // a piece of fewer than four tiles
             pend = {true, valid, r_group, 0, gi, (uint32_t)(t.q & 1), slot_of(p, t.seg, worker), m_run, l_run};
+            pend_rows = max(0, min(sg.tph, rows_in_group(p, t.rg) / p.G - sg.t0)) * p.G;
         }
         ++gi;
     }
-    if (pend.on && ok) write_record(4);
+    // The last piece's record: rows staged in shared memory (the ring is idle:
+    // every tile of this CTA has landed and been consumed), written with one
+    // bulk store, after which this CTA arrives on the grid barrier. Every
+    // softmax thread reaches the named barrier once, whatever happened before;
+    // a timeout anywhere (abort set) leaves the arrival to the merge phase.
+    bool rec = pend.on && ok && *abort == 0;
+    if (rec) {
+        rec = wait_bar(bar_addr(sh.pv_done[pend.gi & 1]), (pend.gi >> 1) & 1, abort, p.dev_err);
+        if (__all_sync(0xffffffffu, rec)) {
+            tc_fence_after();
+            const uint32_t tOp = tmem + lane_off + kColO + pend.ob * 128;
+            const uint32_t srow = ring + (uint32_t)row * 528u;
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {
+                uint32_t o[32];
+                tmem_ld32(tOp + 32 * k, o);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) sts_v4(srow + (uint32_t)(32 * k + e) * 4u, o[e], o[e + 1], o[e + 2], o[e + 3]);
+            }
+            sts_v2(srow + 512u, pend.m, pend.l);
+            fence_proxy_async_smem();
+        }
+    }
+    named_sync(1, 128);
+    if (tid_wg == 0 && pend.on && *abort == 0) {
+        if (pend_rows > 0)
+            bulk_store(p.ws_rec + (pend.slot * p.rows_pg + sg.t0 * p.G) * 132, ring, (uint32_t)pend_rows * 528u);
+        bulk_store_commit_and_wait();
+        fence_proxy_async_all();
+        __threadfence();
+        atomicAdd(&p.bar[0], 1u);
+        sh.arrived = 1;
+    }
 }
 
 // kGeneric: K/V stored in any layout but contiguous head-major (4-D maps,
-// paged pools)
-template <int kStages, bool kGeneric = false>
-__global__ void __launch_bounds__(kThreads, 1)
+// paged pools). kCS: CTAs per cluster, fixed at compile time so that the
+// cluster shape is part of the kernel itself and every launch of it, by any
+// launcher, runs as clusters of kCS CTAs.
+template <int kStages, bool kGeneric, int kCS>
+__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
     k_tc2_verify(const __grid_constant__ AttnParams p, const __grid_constant__ Tc2Maps maps) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned (128-byte swizzle atoms), by pointer arithmetic on the
@@ -506,8 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every cluster operation below (multicast copies and commits, cluster
     // barriers) assumes a cluster of exactly csize CTAs and one worker per
     // cluster; a launch in any other shape writes nothing and says so.
-    if (p.csize < 2 || p.csize > kMaxCluster || cluster_nctarank() != (uint32_t)p.csize ||
-        gridDim.x != (uint32_t)p.csize * (uint32_t)p.workers) {
+    if (p.csize != kCS || cluster_nctarank() != (uint32_t)kCS || gridDim.x != (uint32_t)kCS * (uint32_t)p.workers) {
         if (threadIdx.x == 0) flag_error(p.dev_err, HTA_DEVERR_LAUNCH);
         return;
     }
@@ -529,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_addr(sh.o_free[1]), 128);
         mbar_init(bar_addr(sh.drain), 1);
         sh.abort = 0;
+        sh.arrived = 0;
         mbar_fence_init();
     }
     if (warp == 0 && (threadIdx.x & 31) == 0) {
@@ -583,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // outside that region, so the CTA leaves only after every CTA of the
     // cluster has come this far
     cluster_arrive();
-    merge_phase<128>(p, lens_s, pre_s, lo_s, smem + kOffQ, off_shared(kStages) - kOffQ);
+    merge_phase<128>(p, lens_s, pre_s, lo_s, smem + kOffQ, off_shared(kStages) - kOffQ, sh.arrived != 0);
     grid_barrier_depart(p);
     cluster_wait();
 }
@@ -602,46 +639,59 @@ int tc2_stages(int B, int workers) {
     return 0;
 }
 
-template <int kStages, bool kGeneric>
-cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cudaStream_t stream) {
-    const size_t smem = tc2_smem_bytes(kStages, p.B, grid / p.csize);
-    cudaError_t e = cudaFuncSetAttribute(k_tc2_verify<kStages, kGeneric>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+// The cluster shape comes from the kernel's compile-time cluster dimensions;
+// the launch adds a cooperative grid (the merge waits on every CTA) and
+// programmatic serialization.
+template <int kStages, bool kGeneric, int kCS>
+cudaError_t launch_cs(const AttnParams &p, const Tc2Maps &maps, int grid, cudaStream_t stream) {
+    const size_t smem = tc2_smem_bytes(kStages, p.B, grid / kCS);
+    cudaError_t e = cudaFuncSetAttribute(k_tc2_verify<kStages, kGeneric, kCS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[3];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)p.csize;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    return launch_dependent(cfg, attr, 2, k_tc2_verify<kStages, kGeneric>, p, maps);
+    return launch_dependent(cfg, attr, 1, k_tc2_verify<kStages, kGeneric, kCS>, p, maps);
+}
+
+template <int kStages, bool kGeneric>
+cudaError_t launch_stages(const AttnParams &p, const Tc2Maps &maps, int grid, cudaStream_t stream) {
+    switch (p.csize) {
+        case 2: return launch_cs<kStages, kGeneric, 2>(p, maps, grid, stream);
+        case 3: return launch_cs<kStages, kGeneric, 3>(p, maps, grid, stream);
+        case 4: return launch_cs<kStages, kGeneric, 4>(p, maps, grid, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int kStages, int kCS>
+int max_clusters_cs(int B, int num_sms) {
+    const size_t smem = tc2_smem_bytes(kStages, B, num_sms / 2);
+    if (cudaFuncSetAttribute(k_tc2_verify<kStages, false, kCS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((num_sms / kCS) * kCS);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void *)k_tc2_verify<kStages, false, kCS>, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 template <int kStages>
 int max_clusters(int B, int num_sms, int csize) {
-    const size_t smem = tc2_smem_bytes(kStages, B, num_sms / 2);
-    if (cudaFuncSetAttribute(k_tc2_verify<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((num_sms / csize) * csize);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (void *)k_tc2_verify<kStages>, &cfg) != cudaSuccess) return 0;
-    return n;
+    switch (csize) {
+        case 2: return max_clusters_cs<kStages, 2>(B, num_sms);
+        case 3: return max_clusters_cs<kStages, 3>(B, num_sms);
+        case 4: return max_clusters_cs<kStages, 4>(B, num_sms);
+    }
+    return 0;
 }
 
 }  // namespace

@@ -29,7 +29,8 @@ KV_HND, KV_NHD = 0, 1
 TMAX, BMAX = 256, 1024
 
 # every exported symbol of include/hta.h
-EXPORTS = ("hta_build_mask", "hta_workspace_bytes", "hta_prefix_attn", "hta_tree_attn",
+EXPORTS = ("hta_build_mask", "hta_verify_workspace_bytes", "hta_workspace_bytes", "hta_prefix_attn",
+           "hta_tree_attn",
            "hta_merge", "hta_verify", "hta_verify_noalloc", "hta_accept_commit", "hta_window_attn",
            "hta_logitspec_tree", "hta_verify_kv", "hta_prefix_attn_kv", "hta_accept_commit_kv",
            "hta_status_string",
@@ -71,6 +72,8 @@ def load():
         P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         D = ctypes.POINTER(HtaDims)
         lib.hta_build_mask.argtypes = [P, I32, I32, P, P, P]
+        lib.hta_verify_workspace_bytes.argtypes = [D, P]
+        lib.hta_verify_workspace_bytes.restype = SZ
         lib.hta_workspace_bytes.argtypes = [D]
         lib.hta_workspace_bytes.restype = SZ
         lib.hta_prefix_attn.argtypes = [D, P, P, P, P, P, P, P, SZ, P, P]
@@ -132,8 +135,16 @@ def dims_of(q, k_cache, scale: float = 0.0) -> HtaDims:
     return HtaDims(B, T, Hq, Hkv, d, Lmax, float(scale))
 
 
-def workspace_bytes(dims: HtaDims) -> int:
-    return int(load().hta_workspace_bytes(ctypes.byref(dims)))
+def workspace_bytes(dims: HtaDims, host_cache_lens=None) -> int:
+    """hta_verify_workspace_bytes: host_cache_lens is None (bound over every
+    length <= Lmax) or a host int32 array of the B cache lengths."""
+    if host_cache_lens is None:
+        return int(load().hta_verify_workspace_bytes(ctypes.byref(dims), None))
+    import numpy as np
+    lens = np.ascontiguousarray(host_cache_lens, dtype=np.int32)
+    if lens.shape != (dims.B,):
+        raise ValueError("host_cache_lens must hold B lengths")
+    return int(load().hta_verify_workspace_bytes(ctypes.byref(dims), lens.ctypes.data))
 
 
 def workspace(dims: HtaDims, device) -> torch.Tensor:
@@ -230,13 +241,21 @@ def verify(q, k_cache, v_cache, cache_lens, k_spec, v_spec, mask, *, scale: floa
 
 
 def prefix_attn(q, k_cache, v_cache, cache_lens, *, scale: float = 0.0,
-                ws: torch.Tensor | None = None, dev_err: torch.Tensor | None = None):
-    """Cached part alone. Returns (o_c fp32 [B][T][Hq][d], lse_c fp32 [B][T][Hq])."""
+                ws: torch.Tensor | None = None, dev_err: torch.Tensor | None = None, out: tuple | None = None):
+    """Cached part alone. Returns (o_c fp32 [B][T][Hq][d], lse_c fp32 [B][T][Hq]),
+    written into `out` when given."""
     _check_qkv(q, k_cache, v_cache, cache_lens)
     dims = dims_of(q, k_cache, scale)
     dev = q.device
-    o_c = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    lse_c = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    if out is None:
+        o_c = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        lse_c = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    else:
+        o_c, lse_c = out
+        _check(o_c, "o_c", torch.float32, 4, dev)
+        _check(lse_c, "lse_c", torch.float32, 3, dev)
+        if o_c.shape != q.shape or lse_c.shape != q.shape[:3]:
+            raise ValueError("out must be (o_c [B][T][Hq][d], lse_c [B][T][Hq])")
     if ws is None:
         ws = workspace(dims, dev)
     with torch.cuda.device(dev):

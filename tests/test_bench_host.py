@@ -1,9 +1,8 @@
-"""Host-side logic of bench.py, on CPU: the multi-rank aggregation (gloo,
-world size 2), the clock-sample parser, the byte counts and the reference
-arm's JSON line."""
+"""Host-side logic of bench.py, on CPU: the single-GPU guard (a run asked
+for more GPUs prints one skip line and does no GPU work), the clock-sample
+parser, the byte counts and the reference arm's JSON line."""
 import json
 import os
-import socket
 import subprocess
 import sys
 
@@ -16,45 +15,34 @@ import bench  # noqa: E402
 from speculative_decoding_tree_hybrid_gb300 import workloads as wl  # noqa: E402
 
 
-def _free_port():
-    s = socket.socket()
-    s.bind(("127.0.0.1", 0))
-    port = s.getsockname()[1]
-    s.close()
-    return port
-
-
-def _worker(rank, world, port, q):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
-    import torch.distributed as dist
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    # rank r processed 10 units in r+1 seconds: the job rate is 2*10 / 2 s
-    value, t = bench.aggregate(10.0, float(rank + 1), dist)
-    bench.barrier(dist)
-    q.put((rank, value, t))
-    dist.destroy_process_group()
-
-
-def test_aggregate_two_gloo_ranks():
-    import torch.multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=120)
-        assert p.exitcode == 0
-    res = sorted(q.get(timeout=10) for _ in range(2))
-    for rank, value, t in res:
-        assert t == 2.0 and value == pytest.approx(10.0)
-
-
-def test_aggregate_single_process():
-    v, t = bench.aggregate(6.0, 3.0, None)
+def test_throughput():
+    v, t = bench.throughput(6.0, 3.0)
     assert v == 2.0 and t == 3.0
+
+
+@pytest.mark.parametrize("env,args", [({"WORLD_SIZE": "2", "RANK": "0"}, []), ({}, ["--gpus", "4"])])
+def test_multi_gpu_run_prints_one_skip_line(env, args):
+    """More than one GPU: no GPU work, one JSON line with the reason (rank 0)."""
+    e = dict(os.environ, **env)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args, "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT, env=e)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["skipped"] and line["value"] is None and line["n_gpus"] > 1
+
+
+def test_multi_gpu_other_ranks_print_nothing():
+    e = dict(os.environ, WORLD_SIZE="2", RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT, env=e)
+    assert out.returncode == 0, out.stderr
+    assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
 
 
 def test_clock_summary_parser():

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for required in ("hta_build_mask", "hta_prefix_attn", "hta_tree_attn", "hta_merge",
-                     "hta_verify", "hta_workspace_bytes", "hta_status_string"):
+                     "hta_verify", "hta_verify_workspace_bytes", "hta_status_string"):
         assert required in names
     assert set(names) == set(hta.EXPORTS)
 
@@ -95,6 +95,34 @@ def test_workspace_query_without_device_is_zero_or_sized(lib):
     n = hta.workspace_bytes(_dims())
     assert n == 0 or n >= 256
     assert hta.workspace_bytes(_dims(d=96)) == 0
+
+
+def test_verify_workspace_bytes_signature(lib):
+    """hta_verify_workspace_bytes(dims, host_cache_lens): NULL bounds every
+    length <= Lmax; host lengths give a size no larger than that bound; the
+    old name is the NULL form."""
+    import numpy as np
+    d = _dims(B=2, Lmax=4096)
+    lens = np.array([100, 4096], np.int32)
+    bound = int(lib.hta_verify_workspace_bytes(ctypes.byref(d), None))
+    sized = int(lib.hta_verify_workspace_bytes(ctypes.byref(d), lens.ctypes.data))
+    assert bound == int(lib.hta_workspace_bytes(ctypes.byref(d)))
+    assert sized <= bound
+    assert hta.workspace_bytes(d, lens) == sized and hta.workspace_bytes(d) == bound
+    with pytest.raises(ValueError):
+        hta.workspace_bytes(d, np.zeros(3, np.int32))
+    assert int(lib.hta_verify_workspace_bytes(None, None)) == 0
+
+
+def test_verify_refuses_memory_that_is_not_on_the_current_device(lib):
+    """Valid dims, aligned pointers that are not device allocations of the
+    current device (or no device at all): refused on the host with
+    HTA_ERR_INVALID_ARG before any launch."""
+    d = _dims()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.hta_verify(ctypes.byref(d), *([fake] * 10), 1 << 20, None, None) == -1
+    assert lib.hta_prefix_attn(ctypes.byref(d), *([fake] * 7), 1 << 20, None, None) == -1
+    assert lib.hta_tree_attn(ctypes.byref(d), *([fake] * 6), None) == -1
 
 
 def test_binding_refuses_host_tensors():
