@@ -318,67 +318,169 @@ __device__ __forceinline__ int64_t slot_of(const AttnParams &p, int64_t seg, int
     return (seg + w) * p.subs + x;
 }
 
-// ---------------------------------------------------------------- merge phase
+// ---------------------------------------------------------------- merge
+
+// Pieces of segment `seg` of sequence b: the workers that cover its units
+// (first worker cf, np of them, ne of them with a record; a worker with an
+// empty range writes none). np = 0 for a segment without units.
+struct SegPieces {
+    int32_t cf, np, ne;
+};
+
+__device__ __forceinline__ SegPieces seg_pieces(const AttnParams &p, uint32_t seg, const int32_t *lens_s,
+                                                const int64_t *pre_s, const int64_t *lo_s) {
+    SegPieces r = {0, 0, 0};
+    const uint32_t segs_per_b = (uint32_t)(p.Hkv * p.n_rg);
+    const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
+    const int32_t su = seg_units(p, lens_s[b]);
+    if (su <= 0) return r;
+    const int64_t u0 = pre_s[b] + (int64_t)sl * su;
+    r.cf = cta_of_unit(u0, lo_s, p.workers);
+    r.np = cta_of_unit(u0 + su - 1, lo_s, p.workers) - r.cf + 1;
+    for (int32_t k = 0; k < r.np; ++k) r.ne += lo_s[r.cf + k] != lo_s[r.cf + k + 1];
+    return r;
+}
+
+// Merges rows [lo, lo + nrows) of segment seg over its pieces and writes O
+// and LSE: one thread per (row, column chunk) reads the records of every
+// piece straight from global memory (one round trip of independent loads;
+// the records are L2-resident) and applies, pieces in index order, the
+// log-sum-exp merge of the method ("LongSpec: Long-Context Lossless
+// Speculative Decoding with Efficient Drafting and Verification", Korean
+// summary section 2.C "aggregation") in its running form:
+//   M = running max of m_k; when it grows, the sums so far are scaled by
+//   2^(M_old - M_new); w_k = 2^(m_k - M), den += w_k l_k, acc += w_k O_k;
+//   O = acc / den, LSE = (M + log2 den) ln 2.
+// The result depends on the piece order only, not on which CTA merges.
+// ok = false writes NaN (a piece is missing).
+template <int D, int KB>
+__device__ inline void merge_rows(const AttnParams &p, const int64_t *lo_s, uint32_t seg, const SegPieces &pc,
+                                  uint32_t lo, uint32_t nrows_run, bool ok) {
+    constexpr int HPL = D / 16;  // output columns per thread
+    constexpr int REC = D + 4;   // floats per record: O | m | l | w | pad
+    constexpr int NCH = D / HPL; // column chunks per row (16)
+    const uint32_t rows_pg = (uint32_t)p.rows_pg, n_rg = (uint32_t)p.n_rg;
+    const uint32_t segs_per_b = (uint32_t)p.Hkv * n_rg;
+    const uint32_t G = (uint32_t)p.G, T = (uint32_t)p.T, Hq = (uint32_t)p.Hq;
+    const int32_t subs = p.subs, cf = pc.cf, nrec = pc.np * subs;
+    const bool dense = pc.ne == pc.np;  // every piece has a record: no per-piece checks below
+    const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
+    const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
+    // record x of piece k, row lr: ws_rec + ((seg + cf + k) * subs + x) * rows_pg + lr) * REC
+    const float *const rec0 = p.ws_rec + ((size_t)(seg + cf) * subs * rows_pg) * REC;
+    const size_t rec_stride = (size_t)rows_pg * REC;  // floats between consecutive records
+    for (int32_t item = threadIdx.x; item < (int32_t)nrows_run * NCH; item += blockDim.x) {
+        const int32_t i = item / NCH, ch = item - i * NCH;
+        const uint32_t lr = lo + (uint32_t)i;
+        const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
+        const uint32_t t = r / G, hq = kvh * G + (r - t * G);
+        const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
+        const int col0 = ch * 4;  // this thread's columns: col0 + 64 h + e, h < HPL / 4, e < 4
+        float M = -INFINITY, den = 0.f, acc[HPL];
+#pragma unroll
+        for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
+        if (ok) {
+            const float *row = rec0 + (size_t)lr * REC;
+            // records in batches of KB, every load of a batch issued before any
+            // arithmetic: one round trip per batch (KB is set by the kernel's
+            // register budget)
+            for (int32_t k0 = 0; k0 < nrec; k0 += KB) {
+                float2 ml[KB];
+                float4 v[KB][HPL / 4];
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    const int32_t k = k0 + j;
+                    const bool has = k < nrec && (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1]);
+                    const float *rec = row + (size_t)k * rec_stride;
+                    ml[j] = has ? __ldcg(reinterpret_cast<const float2 *>(rec + D)) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                    for (int c = 0; c < HPL / 4; ++c)
+                        v[j][c] = has ? __ldcg(reinterpret_cast<const float4 *>(rec + col0 + c * 64))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    if (ml[j].x > M) {  // a larger running max: scale what has been summed so far
+                        const float s = M == -INFINITY ? 0.f : tc::ex2(M - ml[j].x);
+                        den *= s;
+#pragma unroll
+                        for (int c = 0; c < HPL; ++c) acc[c] *= s;
+                        M = ml[j].x;
+                    }
+                    const float w = ml[j].x == -INFINITY ? 0.f : tc::ex2(ml[j].x - M);  // no record: no weight
+                    den = fmaf(w, ml[j].y, den);
+#pragma unroll
+                    for (int c = 0; c < HPL / 4; ++c) {
+                        acc[4 * c] = fmaf(w, v[j][c].x, acc[4 * c]);
+                        acc[4 * c + 1] = fmaf(w, v[j][c].y, acc[4 * c + 1]);
+                        acc[4 * c + 2] = fmaf(w, v[j][c].z, acc[4 * c + 2]);
+                        acc[4 * c + 3] = fmaf(w, v[j][c].w, acc[4 * c + 3]);
+                    }
+                }
+            }
+        }
+        float lse, inv;
+        if (!ok) {
+            lse = __int_as_float(0x7fc00000);
+            inv = __int_as_float(0x7fc00000);
+        } else if (den > 0.f) {
+            float l2;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(den));
+            lse = (M + l2) * kLn2;
+            inv = __frcp_rn(den);
+        } else {
+            lse = -INFINITY;  // no visible key: empty softmax
+            inv = 0.f;
+        }
+        if (p.out_fp32) {
+            float *op = (float *)p.out_o + out_row * D + col0;
+#pragma unroll
+            for (int c = 0; c < HPL; c += 4)
+                *reinterpret_cast<float4 *>(op + c * 16) =
+                    make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
+        } else {
+            __nv_bfloat16 *op = (__nv_bfloat16 *)p.out_o + out_row * D + col0;
+#pragma unroll
+            for (int c = 0; c < HPL; c += 4) {
+                const __nv_bfloat162 x = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
+                const __nv_bfloat162 y = __floats2bfloat162_rn(acc[c + 2] * inv, acc[c + 3] * inv);
+                uint2 u;
+                u.x = *reinterpret_cast<const uint32_t *>(&x);
+                u.y = *reinterpret_cast<const uint32_t *>(&y);
+                *reinterpret_cast<uint2 *>(op + c * 16) = u;
+            }
+        }
+        if (ch == 0) p.out_lse[out_row] = lse;
+    }
+}
 
 // Merges every output row handled by this CTA, after a grid-wide barrier
-// that it enters here. Rows are the packed rows of all segments, linearised
-// segment-major and split evenly over the grid (the host keeps every row and
-// unit count below 2^31, so 32-bit index math is exact). The CTA's slice is
-// cut into runs, one per segment it touches; between its arrival at the
-// barrier and the wait, one thread per run locates the run's pieces (the CTAs
-// that covered the segment), so that index math overlaps the barrier. Then,
-// chunk by chunk, the lanes of warp 0 bulk-copy the chunk's records of every
-// piece (contiguous per piece) into shared memory, all copies in flight on
-// one mbarrier (the copy engine keeps far more bytes in flight than per-thread
-// loads), and one thread per (row, column chunk) applies
-//   M = max_k m_k, w_k = 2^(m_k - M), O = sum_k w_k O_k / sum_k w_k l_k,
-//   LSE = (M + log2 sum_k w_k l_k) ln 2,
-// the log-sum-exp merge of the method ("LongSpec: Long-Context Lossless
-// Speculative Decoding with Efficient Drafting and Verification", Korean
-// summary section 2.C "aggregation").
-// `buf` is idle shared memory (the run table, then the staged records); the
-// block has more than kMergeRuns threads.
+// that it enters here (kernels launched as cooperative grids). Rows are the
+// packed rows of all segments, linearised segment-major and split evenly
+// over the grid (the host keeps every row and unit count below 2^31, so
+// 32-bit index math is exact). The CTA's slice is cut into runs, one per
+// segment it touches; between its arrival at the barrier and the wait, one
+// thread per run locates the run's pieces, so that index math overlaps the
+// barrier; each run is then merged by merge_rows.
+// `buf` is idle shared memory for the run table; the block has more than
+// kMergeRuns threads. `arrived`: this CTA has already arrived on the barrier.
 constexpr int kMergeRuns = 64;
-constexpr uint32_t kMergePlanBytes = 6 * kMergeRuns * 4 + 16;  // run table, copy mbarrier, status
 
-template <int D>
+template <int D, int KB>
 __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, const int64_t *pre_s,
-                                   const int64_t *lo_s, uint8_t *buf, uint32_t buf_bytes, bool arrived = false) {
-    constexpr int HPL = D / 16;                 // columns per lane of a half-warp
-    constexpr int REC = D + 4;                  // floats per record: O | m | l | w | pad
-    constexpr uint32_t REC_BYTES = REC * 4;
+                                   const int64_t *lo_s, uint8_t *buf, bool arrived = false) {
     const uint32_t grid = gridDim.x;
-    const int32_t workers = p.workers;
     const uint32_t rows_pg = (uint32_t)p.rows_pg, n_rg = (uint32_t)p.n_rg, hkv = (uint32_t)p.Hkv;
     const uint32_t segs_per_b = hkv * n_rg;
-    // launch parameters used per row, read once
-    const uint32_t G = (uint32_t)p.G, T = (uint32_t)p.T, Hq = (uint32_t)p.Hq;
-    const bool out_fp32 = p.out_fp32 != 0;
-    void *const out_o = p.out_o;
-    float *const out_lse = p.out_lse;
-    const float *const ws_rec = p.ws_rec;
-    const int32_t subs = p.subs;
     const uint32_t rows_total = (uint32_t)p.B * segs_per_b * rows_pg;
     const uint32_t r0 = (uint32_t)(((uint64_t)blockIdx.x * rows_total) / grid);
     const uint32_t r1 = (uint32_t)(((uint64_t)(blockIdx.x + 1) * rows_total) / grid);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *run_seg = reinterpret_cast<int32_t *>(buf);
-    int32_t *run_cf = run_seg + kMergeRuns;  // first piece (CTA index)
+    int32_t *run_cf = run_seg + kMergeRuns;  // first piece (worker index)
     int32_t *run_np = run_cf + kMergeRuns;   // pieces
     int32_t *run_lo = run_np + kMergeRuns;   // first local row
     int32_t *run_nr = run_lo + kMergeRuns;   // rows
-    int32_t *run_ne = run_nr + kMergeRuns;   // pieces with a record (an empty worker range writes none)
-    uint8_t *stage = buf + kMergePlanBytes;
-    const uint32_t stage_bytes = buf_bytes - kMergePlanBytes;
-    const uint32_t stage_u32 = tc::smem_u32(stage);
-    const uint32_t bar = tc::smem_u32(buf + 6 * kMergeRuns * 4);
-    volatile int32_t *staged_s = reinterpret_cast<volatile int32_t *>(buf + 6 * kMergeRuns * 4 + 8);
-    uint32_t phase = 0;
-    if (threadIdx.x == 0) {
-        tc::mbar_init(bar, 1);
-        tc::mbar_fence_init();
-    }
-
+    int32_t *run_ne = run_nr + kMergeRuns;   // pieces with a record
     if (!arrived) grid_barrier_arrive(p);
     else __syncthreads();
     bool ok = true, waited = false;
@@ -387,26 +489,19 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
         const uint32_t n_runs = sb < seg_end ? min((uint32_t)kMergeRuns, seg_end - sb) : 0u;
         if (threadIdx.x < n_runs) {
             const uint32_t seg = sb + threadIdx.x;
-            const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
+            const uint32_t sl = seg % segs_per_b;
             const uint32_t nrows = (uint32_t)rows_in_group(p, (int32_t)(sl % n_rg));
             const uint32_t base = seg * rows_pg;
             const uint32_t lo = (r0 > base ? r0 : base) - base;
             const uint32_t hi = min(r1 - base, nrows);
-            const int32_t su = seg_units(p, lens_s[b]);
-            int32_t cf = 0, np = 0;
-            if (su > 0 && hi > lo) {
-                const int64_t u0 = pre_s[b] + (int64_t)sl * su;
-                cf = cta_of_unit(u0, lo_s, workers);
-                np = cta_of_unit(u0 + su - 1, lo_s, workers) - cf + 1;
-            }
+            SegPieces pc = {0, 0, 0};
+            if (hi > lo) pc = seg_pieces(p, seg, lens_s, pre_s, lo_s);
             run_seg[threadIdx.x] = (int32_t)seg;
-            run_cf[threadIdx.x] = cf;
-            run_np[threadIdx.x] = np;
+            run_cf[threadIdx.x] = pc.cf;
+            run_np[threadIdx.x] = pc.np;
             run_lo[threadIdx.x] = (int32_t)lo;
             run_nr[threadIdx.x] = hi > lo ? (int32_t)(hi - lo) : 0;
-            int32_t ne = 0;
-            for (int32_t k = 0; k < np; ++k) ne += lo_s[cf + k] != lo_s[cf + k + 1];
-            run_ne[threadIdx.x] = ne;
+            run_ne[threadIdx.x] = pc.ne;
         }
         if (!waited) {
             ok = grid_barrier_wait(p);  // its closing __syncthreads also publishes the table
@@ -414,128 +509,9 @@ __device__ inline void merge_phase(const AttnParams &p, const int32_t *lens_s, c
         } else {
             __syncthreads();
         }
-
         for (uint32_t j = 0; j < n_runs; ++j) {
-            const uint32_t seg = (uint32_t)run_seg[j];
-            const int32_t cf = run_cf[j], np = run_np[j], nrows_run = run_nr[j], ne = run_ne[j];
-            const bool dense = ne == np;  // every piece has a record: no per-piece checks below
-            const uint32_t b = seg / segs_per_b, sl = seg - b * segs_per_b;
-            const uint32_t kvh = sl / n_rg, rg = sl - kvh * n_rg;
-            // rows per chunk: every record of the chunk fits in `stage`
-            const uint32_t per_row = (uint32_t)(np > 0 ? np * subs : 1) * REC_BYTES;
-            const int32_t cap = (int32_t)(stage_bytes / per_row) > 0 ? (int32_t)(stage_bytes / per_row) : 1;
-            for (int32_t c0 = 0; c0 < nrows_run; c0 += cap) {
-                const int32_t nr = min(cap, nrows_run - c0);
-                const uint32_t lr0 = (uint32_t)(run_lo[j] + c0);
-                // record x of piece k, rows lr0 .. lr0+nr-1 -> stage + (k * subs + x) * nr * REC_BYTES
-                const uint32_t bytes = (uint32_t)nr * REC_BYTES;
-                if (ok && warp == 0 && np > 0) {
-                    // the records were written through the generic proxy by other CTAs
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)(ne * subs) * bytes);
-                    for (int32_t kx = lane; kx < np * subs; kx += 32) {
-                        const int32_t k = kx / subs;
-                        if (!dense && lo_s[cf + k] == lo_s[cf + k + 1]) continue;
-                        const float *src = ws_rec + ((size_t)((seg + cf + k) * subs + (kx - k * subs)) * rows_pg + lr0) * REC;
-                        tc::bulk_load(stage_u32 + (uint32_t)kx * bytes, src, bytes, bar);
-                    }
-                }
-                if (threadIdx.x == 0) {
-                    int32_t st = 1;
-                    if (ok && np > 0) {
-                        const uint64_t t0 = cycles_now();
-                        while (!tc::mbar_try_wait(bar, phase)) {
-                            if (cycles_now() - t0 > kWaitLimitCycles) {
-                                flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
-                                st = 0;
-                                break;
-                            }
-                        }
-                    }
-                    *staged_s = st;
-                }
-                if (ok && np > 0) phase ^= 1;
-                __syncthreads();
-                ok = ok && *staged_s != 0;  // a timed-out copy leaves NaN outputs from here on
-                const uint32_t pstride = (uint32_t)nr * REC;  // floats between records
-                const int32_t nrec = np * subs;
-                // one thread per (row, 8-column chunk, or 4 for d = 64): each
-                // computes the piece weights of its row itself (broadcast
-                // shared-memory reads) and its own output columns, so every
-                // load of the chunk is independent of the others
-                constexpr int NCH = D / HPL;  // column chunks per row (16)
-                for (int32_t item = threadIdx.x; item < nr * NCH; item += blockDim.x) {
-                    const int32_t i = item / NCH, ch = item - i * NCH;
-                    const uint32_t lr = lr0 + (uint32_t)i;
-                    const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
-                    const uint32_t t = r / G, hq = kvh * G + (r - t * G);
-                    const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
-                    // the staged records are read with shared-memory loads on their
-                    // shared-window address (a generic access costs a global-load latency)
-                    const uint32_t row0 = stage_u32 + (uint32_t)i * REC_BYTES;
-                    const int col0 = ch * 4;  // this thread's columns: col0 + 64 h + e, h < HPL / 4, e < 4
-                    float M = -INFINITY;
-                    for (int32_t k = 0; k < nrec; ++k)
-                        if (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1])
-                            M = fmaxf(M, tc::lds_f32(row0 + ((uint32_t)k * pstride + D) * 4u));
-                    float den = 0.f, acc[HPL];
-#pragma unroll
-                    for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
-                    if (ok) {
-#pragma unroll 2
-                        for (int32_t k = 0; k < nrec; ++k) {
-                            if (!dense && lo_s[cf + k / subs] == lo_s[cf + k / subs + 1]) continue;  // no record
-                            const uint32_t rec = row0 + (uint32_t)k * pstride * 4u;
-                            const float2 ml = tc::lds_f32x2(rec + D * 4u);
-                            const float w = tc::ex2(ml.x - M);
-                            den = fmaf(w, ml.y, den);
-#pragma unroll
-                            for (int c = 0; c < HPL; c += 4) {
-                                // columns 4 ch .. 4 ch + 3 of each 64-column half: the
-                                // lanes of a quarter-warp read 128 contiguous bytes
-                                const float4 v = tc::lds_f32x4(rec + (uint32_t)(col0 + c * 16) * 4u);
-                                acc[c] = fmaf(w, v.x, acc[c]);
-                                acc[c + 1] = fmaf(w, v.y, acc[c + 1]);
-                                acc[c + 2] = fmaf(w, v.z, acc[c + 2]);
-                                acc[c + 3] = fmaf(w, v.w, acc[c + 3]);
-                            }
-                        }
-                    }
-                    float lse, inv;
-                    if (!ok) {
-                        lse = __int_as_float(0x7fc00000);
-                        inv = __int_as_float(0x7fc00000);
-                    } else if (den > 0.f) {
-                        float l2;
-                        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(den));
-                        lse = (M + l2) * kLn2;
-                        inv = __frcp_rn(den);
-                    } else {
-                        lse = -INFINITY;  // no visible key: empty softmax
-                        inv = 0.f;
-                    }
-                    if (out_fp32) {
-                        float *op = (float *)out_o + out_row * D + col0;
-#pragma unroll
-                        for (int c = 0; c < HPL; c += 4)
-                            *reinterpret_cast<float4 *>(op + c * 16) =
-                                make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
-                    } else {
-                        __nv_bfloat16 *op = (__nv_bfloat16 *)out_o + out_row * D + col0;
-#pragma unroll
-                        for (int c = 0; c < HPL; c += 4) {
-                            const __nv_bfloat162 x = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
-                            const __nv_bfloat162 y = __floats2bfloat162_rn(acc[c + 2] * inv, acc[c + 3] * inv);
-                            uint2 u;
-                            u.x = *reinterpret_cast<const uint32_t *>(&x);
-                            u.y = *reinterpret_cast<const uint32_t *>(&y);
-                            *reinterpret_cast<uint2 *>(op + c * 16) = u;
-                        }
-                    }
-                    if (ch == 0) out_lse[out_row] = lse;
-                }
-                __syncthreads();  // the stage is refilled by the next chunk
-            }
+            const SegPieces pc = {run_cf[j], run_np[j], run_ne[j]};
+            merge_rows<D, KB>(p, lo_s, (uint32_t)run_seg[j], pc, (uint32_t)run_lo[j], (uint32_t)run_nr[j], ok);
         }
         __syncthreads();  // the run table is rewritten by the next batch
     }

@@ -163,9 +163,9 @@ __global__ void __launch_bounds__(kThreads) k_cc_attn(const __grid_constant__ At
         cc_emit<D>(p, st, pos.seg, pos.b, pos.kvh, pos.rg, slot_of(p, pos.seg, blockIdx.x), false);
         u = piece_end;
     }
-    __syncthreads();  // the tile buffers stage the merge
-    static_assert(sizeof(CcSmem<D>) >= kMergePlanBytes + 32 * (D + 4) * 4, "merge stage too small");
-    merge_phase<D>(p, lens_s, pre_s, lo_s, smem_raw, (uint32_t)sizeof(CcSmem<D>));
+    __syncthreads();  // the tile buffers hold the merge's run table
+    static_assert(sizeof(CcSmem<D>) >= 6 * kMergeRuns * 4, "no room for the merge's run table");
+    merge_phase<D, 4>(p, lens_s, pre_s, lo_s, smem_raw);
     grid_barrier_depart(p);
 }
 

@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
     // Q and the K/V ring are idle now: they stage the merge
-    merge_phase<128>(p, lens_s, pre_s, lo_s, smem + kOffQ, off_shared(kStages) - kOffQ);
+    merge_phase<128, 2>(p, lens_s, pre_s, lo_s, smem + kOffQ);  // 2 records per round trip: the register budget of 384 threads
     grid_barrier_depart(p);
 }
 

@@ -620,7 +620,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
     // outside that region, so the CTA leaves only after every CTA of the
     // cluster has come this far
     cluster_arrive();
-    merge_phase<128>(p, lens_s, pre_s, lo_s, smem + kOffQ, off_shared(kStages) - kOffQ, sh.arrived != 0);
+    merge_phase<128, 12>(p, lens_s, pre_s, lo_s, smem + kOffQ, sh.arrived != 0);  // 12 records per round trip
     grid_barrier_depart(p);
     cluster_wait();
 }
