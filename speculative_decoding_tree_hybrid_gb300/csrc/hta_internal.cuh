@@ -257,7 +257,7 @@ __device__ __forceinline__ int32_t rows_in_group(const AttnParams &p, int32_t rg
 
 // ---------------------------------------------------------------- barrier
 
-// Grid-wide barrier for a cooperative launch (every CTA is resident), split
+// Grid-wide barrier for a persistent grid (every CTA is resident), split
 // in two so that a CTA can do independent work between its arrival and the
 // wait. The wait is bounded (p.bar_wait_cycles, ~4 s of device time unless a
 // test sets a shorter bound); on expiry the error flag is set and the barrier
@@ -455,7 +455,7 @@ __device__ inline void merge_rows(const AttnParams &p, const int64_t *lo_s, uint
 }
 
 // Merges every output row handled by this CTA, after a grid-wide barrier
-// that it enters here (kernels launched as cooperative grids). Rows are the
+// that it enters here (persistent grids, every CTA resident). Rows are the
 // packed rows of all segments, linearised segment-major and split evenly
 // over the grid (the host keeps every row and unit count below 2^31, so
 // 32-bit index math is exact). The CTA's slice is cut into runs, one per

@@ -4,10 +4,25 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 
 #include "hta_internal.cuh"
 
 namespace hta {
+
+// The attention kernels merge their split-KV partials after a grid-wide
+// barrier, so every CTA of the grid must be resident at once. Their grids are
+// sized by the occupancy query to fit the device, and none of them lets a
+// dependent start before it has finished (no early launch_dependents: with
+// clusters of three CTAs that measured as a stall), so nothing launched after
+// a grid can hold SMs it needs; they are launched as ordinary grids by
+// default, 2.2 us per call sooner back to back than cooperative ones.
+// HTA_COOPERATIVE=1 (read on every call) asks for a cooperative launch, which
+// also guarantees co-residency against work on other streams.
+inline bool cooperative_requested() {
+    const char *s = getenv("HTA_COOPERATIVE");
+    return s && s[0] == '1' && s[1] == 0;
+}
 
 // Launches `kern` with the n attributes in attrs[0 .. n) plus programmatic
 // stream serialization (attrs must have room for n + 1): the kernel may then

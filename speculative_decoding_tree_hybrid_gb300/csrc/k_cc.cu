@@ -1,6 +1,6 @@
 // CUDA-core (FFMA) path of the hybrid tree attention, for head dimension 64
 // and for trees whose packed query rows are too few to fill a tensor-core
-// tile. One persistent cooperative grid covers both parts of the method
+// tile. One persistent grid (all CTAs resident) covers both parts of the method
 // ("LongSpec: Long-Context Lossless Speculative Decoding with Efficient
 // Drafting and Verification", Korean summary section 2.C: the unmasked cached
 // part and the masked speculative part) as tiles of 64 keys, then merges all
@@ -187,7 +187,7 @@ cudaError_t cc_launch_t(const AttnParams &p, bool direct, int grid, cudaStream_t
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = direct ? 0 : 1;
+    attr[0].val.cooperative = (!direct && cooperative_requested()) ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_cc_attn<D>, p, direct ? 1 : 0);

@@ -5,7 +5,7 @@
 // summary Methodologie section 3) splits the verification attention into an
 // unmasked pass over the long cached prefix and a masked pass over the tree
 // tokens, merged by log-sum-exp. Here both passes are 128-key tiles of one
-// persistent cooperative grid (one CTA per SM, a static split-KV schedule
+// persistent grid (one CTA per SM, all resident, a static split-KV schedule
 // balanced by tile count, see hta_internal.cuh), and the cross-split and
 // cross-part merge runs after a grid barrier in the same launch.
 //
@@ -523,9 +523,12 @@ cudaError_t launch_stages(const AttnParams &p, const TcMaps &maps, int grid, cud
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    return launch_dependent(cfg, attr, 1, k_tc_verify<kStages, kGeneric>, p, maps);
+    int n = 0;
+    if (cooperative_requested()) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n++].val.cooperative = 1;
+    }
+    return launch_dependent(cfg, attr, n, k_tc_verify<kStages, kGeneric>, p, maps);
 }
 
 }  // namespace

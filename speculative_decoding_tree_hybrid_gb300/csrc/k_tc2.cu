@@ -6,7 +6,7 @@
 // summary Methodologie section 3) splits the verification attention into an
 // unmasked pass over the cached prefix and a masked pass over the tree tokens,
 // merged by log-sum-exp; as in the single-CTA path, both passes are 128-key
-// tiles of one persistent cooperative grid and the cross-split merge runs
+// tiles of one persistent grid (all CTAs resident) and the cross-split merge runs
 // after a grid barrier in the same launch.
 //
 // Here the grid is made of clusters of csize CTAs (2 to 4) on csize SMs. A
@@ -640,8 +640,8 @@ int tc2_stages(int B, int workers) {
 }
 
 // The cluster shape comes from the kernel's compile-time cluster dimensions;
-// the launch adds a cooperative grid (the merge waits on every CTA) and
-// programmatic serialization.
+// the launch adds programmatic serialization (and a cooperative grid when
+// requested: the merge waits on every CTA, see cooperative_requested).
 template <int kStages, bool kGeneric, int kCS>
 cudaError_t launch_cs(const AttnParams &p, const Tc2Maps &maps, int grid, cudaStream_t stream) {
     const size_t smem = tc2_smem_bytes(kStages, p.B, grid / kCS);
@@ -654,9 +654,12 @@ cudaError_t launch_cs(const AttnParams &p, const Tc2Maps &maps, int grid, cudaSt
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    return launch_dependent(cfg, attr, 1, k_tc2_verify<kStages, kGeneric, kCS>, p, maps);
+    int n = 0;
+    if (cooperative_requested()) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n++].val.cooperative = 1;
+    }
+    return launch_dependent(cfg, attr, n, k_tc2_verify<kStages, kGeneric, kCS>, p, maps);
 }
 
 template <int kStages, bool kGeneric>
