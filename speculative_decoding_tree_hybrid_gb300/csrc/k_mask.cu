@@ -28,6 +28,10 @@ __global__ void __launch_bounds__(HTA_TMAX) k_build_mask(const int32_t *__restri
     const int b = blockIdx.x, i = threadIdx.x;
     const int32_t *par = parents + (int64_t)b * T;
     tc::griddep_launch_dependents();  // the attention launch may set up meanwhile
+    // launched as a programmatic dependent: the kernel before it (often the
+    // attention of the previous step, which reads the mask) has finished and
+    // its memory is visible from here on
+    tc::griddep_wait();
     if (i == 0) bad_s = 0;
     __syncthreads();
     int32_t pi = -1;
@@ -63,9 +67,12 @@ __global__ void __launch_bounds__(HTA_TMAX) k_build_mask(const int32_t *__restri
 
 cudaError_t mask_launch(const int32_t *parents, int B, int T, uint32_t *mask, int32_t *dev_err,
                         cudaStream_t stream) {
-    const int threads = ((T + 31) / 32) * 32;
-    k_build_mask<<<B, threads, 0, stream>>>(parents, T, (T + 31) / 32, mask, dev_err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B);
+    cfg.blockDim = dim3(((T + 31) / 32) * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    return launch_dependent(cfg, attr, 0, k_build_mask, parents, T, (T + 31) / 32, mask, dev_err);
 }
 
 }  // namespace hta
