@@ -82,6 +82,20 @@ def test_tree_properties_by_brute_force(seed):
             cur = nxt[0]
             out.append(int(tok[cur]))
 
+    # the g1 branch: nodes 1 .. c form one chain under the root, holding the
+    # history right after the latest match of (last m-1 tokens, x_{i+1})
+    want_g1 = []
+    if len(hist) >= m - 1:
+        g1 = (hist[len(hist) - (m - 1):] if m > 1 else []) + [x1]
+        s1 = brute_latest(g1)
+        if s1 >= 0:
+            want_g1 = hist[s1 + m:s1 + m + keep[0]]
+    c = min(len(want_g1), T - 1)
+    assert tok[1:1 + c].tolist() == want_g1[:c]
+    assert all(par[i] == (0 if i == 1 else i - 1) for i in range(1, 1 + c))
+    if 1 + c < nn and k >= 1:  # the first guess comes right after the g1 chain
+        assert par[1 + c] == 0 and tok[1 + c] == order[1]
+
     for r, g in enumerate(order[1:k + 1], start=1):
         nodes = [i for i in guess_nodes if tok[i] == g and i >= 1]
         if not nodes:

@@ -5,8 +5,9 @@ split-KV partials in a static device array instead of a caller workspace.
 
 Called through the C ABI twice in a row (the array keeps the previous call's
 contents, so the second call checks that nothing stale leaks through) and
-compared with hta_verify on the same inputs, within the parity tolerances of
-the other GPU tests. This file is collected last on purpose.
+compared both with hta_verify and with the fp64 oracle on the same inputs,
+within the parity tolerances of the other GPU tests. This file is collected
+last on purpose.
 """
 import ctypes
 
@@ -46,7 +47,7 @@ def call_noalloc(t, mask, o, lse, err):
     (1, 8, 4, 1, 64, [256], "uniform"),              # tiny shape, CUDA-core path
     (2, 32, 8, 8, 128, [700, 129], "uniform"),       # two sequences of different lengths
 ])
-def test_noalloc_matches_verify_twice(shape):
+def test_noalloc_matches_verify_twice(oracle_mod, shape):
     B, T, Hq, Hkv, d, lens, tree = shape
     outs = []
     for call, seed in enumerate((71, 72)):  # two calls in a row, different inputs
@@ -63,7 +64,12 @@ def test_noalloc_matches_verify_twice(shape):
         assert st == 0, hta.status_string(st)
         assert int(err.item()) == 0
         assert_close(o, lse, o_ref.double().cpu().numpy(), lse_ref.double().cpu().numpy(),
-                     f"no-alloc call {call}")
+                     f"no-alloc call {call} vs hta_verify")
+        ref_mask, bad = oracle_mod.build_mask(inp.parents)
+        assert bad == 0
+        o_or, lse_or = oracle_mod.attention(inp.q, inp.k_cache, inp.v_cache, inp.cache_lens,
+                                            inp.k_spec, inp.v_spec, ref_mask)
+        assert_close(o, lse, o_or, lse_or, f"no-alloc call {call} vs oracle")
         outs.append(o)
     assert not torch.equal(outs[0], outs[1])  # the second call really recomputed
 
