@@ -1,4 +1,4 @@
-"""Benchmark of the hybrid tree attention hot path on one GB300 (or N replicas).
+"""Benchmark of the hybrid tree attention hot path on one GB300.
 
 A step is one pass of the whole hot path over one batch: the tree mask build
 (hta_build_mask) and the fused verification attention (hta_verify: split-KV
@@ -13,8 +13,9 @@ graph (one graph holds one step per cache), so host launch cost stays out of
 the device-timed loop.
 
 Output: one JSON line. `value` is KV-cache GB/s over the timed steps;
-`us_per_layer_call` the median hta_verify duration from CUDA events
-on the launching stream; `roofline` compares that kernel with the measured HBM
+`us_per_layer_call` the average hta_verify duration back to back (CUDA events
+on the launching stream around graph replays of verify launches) and
+`us_per_isolated_launch` the median of single launches after an L2 flush; `roofline` compares that kernel with the measured HBM
 copy bandwidth; `e2e` repeats the measurement through the public API with the
 inputs in pinned host memory (copies inside the timed region); `cpu_baseline`
 times the fp64 CPU oracle on a bounded sample.

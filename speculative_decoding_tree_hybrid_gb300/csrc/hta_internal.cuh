@@ -19,9 +19,8 @@
 // After a grid-wide barrier every CTA merges a slice of all output rows over
 // the pieces of their segment: the log-sum-exp merge of the method ("LongSpec:
 // Long-Context Lossless Speculative Decoding with Efficient Drafting and
-// Verification", Korean summary section 2.C "aggregation"). The records of a
-// slice are contiguous per piece, so one bulk copy per piece stages them in
-// shared memory before the reduction.
+// Verification", Korean summary section 2.C "aggregation"); each thread
+// loads the records of its row and column chunk straight from L2.
 #pragma once
 
 #include <cuda_bf16.h>
