@@ -184,6 +184,21 @@ def test_verify_is_deterministic(path):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("path", ["cc", "tc", "tc2"], indirect=True)
+def test_cooperative_launch_matches_default(oracle_mod, path, monkeypatch):
+    """HTA_COOPERATIVE=1 launches the persistent grids cooperatively instead of
+    as ordinary programmatically dependent grids: same oracle parity and
+    bit-identical outputs (the schedule and the merge order do not depend on
+    the launch mode)."""
+    inp = wl.random_inputs(2, 64, 32, 8, 128, [3000, 1700], seed=19, tree="window8_depth8")
+    o1, l1 = run_verify(inp, path)
+    monkeypatch.setenv("HTA_COOPERATIVE", "1")
+    o2, l2 = run_verify(inp, path)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o_ref, lse_ref = oracle_full(oracle_mod, inp)
+    assert_close(o2, l2, o_ref, lse_ref, f"cooperative {path}")
+
+
 def test_prefix_tree_merge_entry_points(oracle_mod):
     inp = wl.random_inputs(2, 24, 8, 2, 128, [777, 0], seed=13)
     t = to_device(inp, DEV)
