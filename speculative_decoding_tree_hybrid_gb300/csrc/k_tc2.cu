@@ -392,8 +392,7 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
             fence_proxy_async_smem();
         }
         uint32_t sa[64], sb[64];  // raw scores of keys 0..63 and 64..127
-        tmem_ld64(tS, sa);
-        tmem_ld64(tS + 64, sb);
+        tmem_ld128(tS, sa, sb);
         // raw-score max (the scale is positive); masked keys become -inf
         float mx[8];
 #pragma unroll
@@ -431,7 +430,8 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
             m_run = m_new;
         }
         // P = 2^(s * scale * log2 e - m_run), packed to bf16 pairs over the first
-        // 64 columns of this S buffer (all of S is already in registers)
+        // 64 columns of this S buffer (all of S is already in registers), in
+        // 16-column chunks stored as soon as each is complete
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         {
@@ -443,8 +443,9 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
                 const float p0 = ex2(x0), p1 = ex2(x1);
                 add2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                 pk[e] = pack_bf16x2(p0, p1);
+                if (e == 15) tmem_st16(tS, pk);
             }
-            tmem_st32(tS, pk);
+            tmem_st16(tS + 16, pk + 16);
         }
         {
             uint32_t pk[32];
@@ -455,8 +456,9 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
                 const float p0 = ex2(x0), p1 = ex2(x1);
                 add2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                 pk[e] = pack_bf16x2(p0, p1);
+                if (e == 15) tmem_st16(tS + 32, pk);
             }
-            tmem_st32(tS + 32, pk);
+            tmem_st16(tS + 32 + 16, pk + 16);
         }
         if (__any_sync(0xffffffffu, moved && o_valid)) {
             // O is stable once PV of the previous tile has finished (PV of

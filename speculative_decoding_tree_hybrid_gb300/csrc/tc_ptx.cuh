@@ -405,6 +405,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// 128 consecutive columns: four loads in flight, one wait (a = columns 0..63,
+// b = columns 64..127)
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&a)[64], uint32_t (&b)[64]) {
+#define HTA_A8(i) "=r"(a[i + 0]), "=r"(a[i + 1]), "=r"(a[i + 2]), "=r"(a[i + 3]), "=r"(a[i + 4]), "=r"(a[i + 5]), "=r"(a[i + 6]), "=r"(a[i + 7])
+#define HTA_B8(i) "=r"(b[i + 0]), "=r"(b[i + 1]), "=r"(b[i + 2]), "=r"(b[i + 3]), "=r"(b[i + 4]), "=r"(b[i + 5]), "=r"(b[i + 6]), "=r"(b[i + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : HTA_A8(0), HTA_A8(8), HTA_A8(16), HTA_A8(24), HTA_A8(32), HTA_A8(40), HTA_A8(48), HTA_A8(56),
+          HTA_B8(0), HTA_B8(8), HTA_B8(16), HTA_B8(24), HTA_B8(32), HTA_B8(40), HTA_B8(48), HTA_B8(56)
+        : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+        : "memory");
+#undef HTA_A8
+#undef HTA_B8
+}
+
+// 16 consecutive columns from r[0 .. 15]
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 #undef HTA_R8
