@@ -283,8 +283,7 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         uint32_t sa[64], sb[64];  // raw scores of keys 0..63 and 64..127
-        tmem_ld64(tS, sa);
-        tmem_ld64(tS + 64, sb);
+        tmem_ld128(tS, sa, sb);
 
         // raw-score max (the scale is positive); masked keys become -inf
         float mx[8];
@@ -361,8 +360,9 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
                 const float p0 = ex2(x0), p1 = ex2(x1);
                 add2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                 pk[e] = pack_bf16x2(p0, p1);
+                if (e == 15) tmem_st16(tS, pk);
             }
-            tmem_st32(tS, pk);
+            tmem_st16(tS + 16, pk + 16);
         }
         {
             uint32_t pk[32];
@@ -373,8 +373,9 @@ __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uin
                 const float p0 = ex2(x0), p1 = ex2(x1);
                 add2(ls[2 * (e & 1)], ls[2 * (e & 1) + 1], p0, p1);
                 pk[e] = pack_bf16x2(p0, p1);
+                if (e == 15) tmem_st16(tS + 32, pk);
             }
-            tmem_st32(tS + 32, pk);
+            tmem_st16(tS + 32 + 16, pk + 16);
         }
         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_wait_st();
