@@ -482,9 +482,10 @@ __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, ui
         mbar_arrive(bar_addr(sh.p_full[b]));
         o_valid = true;
 
-        if (pend.on && !write_record(1)) break;  // a part of the previous piece's record
+        // a part of the previous piece's record (all of what is left of it at
+        // the end of a piece of fewer than four tiles)
+        if (pend.on && !write_record(t.last ? 4 : 1)) break;
         if (t.last) {
-            if (pend.on && !write_record(4)) break;  // a piece of fewer than four tiles
             pend = {true, valid, r_group, 0, gi, (uint32_t)(t.q & 1), slot_of(p, t.seg, worker), m_run, l_run};
             pend_rows = max(0, min(sg.tph, rows_in_group(p, t.rg) / p.G - sg.t0)) * p.G;
         }
