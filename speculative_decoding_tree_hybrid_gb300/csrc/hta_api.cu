@@ -205,6 +205,22 @@ uint64_t barrier_wait_cycles() {
     return 8000000000ull;
 }
 
+// The largest grid no larger than `grid` (whole clusters on the clustered
+// path) whose workspace layout fits in ws_bytes; 0 when not even one worker
+// fits.
+int fit_grid(const hta_dims *d, int path, int grid, bool tree, size_t ws_bytes) {
+    const Layout L0 = make_layout(d, path, 0, tree);
+    const size_t per_slot = (size_t)L0.rows_pg * (d->d + 4) * sizeof(float);
+    const size_t usable = ws_bytes / kWsAlign * kWsAlign;
+    if (usable <= L0.off_rec || per_slot == 0) return 0;
+    const int64_t slots = (int64_t)((usable - L0.off_rec) / per_slot);
+    const int64_t workers = slots / (L0.subs > 0 ? L0.subs : 1) - L0.n_seg;
+    if (workers < 1) return 0;
+    const int c = path == kPathTC2 ? tc2_csize(d) : 1;
+    const int64_t w = workers < (int64_t)(grid / c) ? workers : grid / c;
+    return (int)(w * c);
+}
+
 AttnParams base_params(const hta_dims *d, const Layout &L) {
     AttnParams p;
     memset(&p, 0, sizeof p);
@@ -256,6 +272,13 @@ hta_status run_attention(const hta_dims *d, const void *q, const void *kc, const
     }
     else
         grid = (int)(max_units < (int64_t)gmax ? (max_units > 0 ? max_units : 1) : gmax);
+    if (!direct && ws && ((uintptr_t)ws % kWsAlign) == 0) {
+        // A workspace sized for shorter lengths than Lmax holds fewer record
+        // slots: run with the workers it holds (fewer workers only matter when
+        // the lengths have more tiles than workers)
+        const int fit = fit_grid(d, path, grid, use_tree, ws_bytes);
+        if (fit > 0 && fit < grid) grid = fit;
+    }
     Layout L = make_layout(d, path, grid, use_tree);
     AttnParams p = base_params(d, L);
     p.csize = path == kPathTC2 ? tc2_csize(d) : 0;

@@ -87,6 +87,51 @@ def test_verify_and_prefix_write_nothing_outside_their_buffers(case, monkeypatch
     assert ws.intact() and oc.intact() and lc.intact()
 
 
+# short lengths in a cache whose Lmax is far longer: the calls size their grid
+# from Lmax, a workspace from the lengths' query holds fewer workers' records
+SIZED_CASES = [
+    (1, 64, 32, 8, 128, [300], 8192, "window8_depth8", "tc2"),
+    (2, 32, 8, 8, 128, [40, 129], 8192, "uniform", "tc"),
+    (3, 16, 8, 2, 64, [0, 30, 100], 4096, "uniform", "cc"),
+]
+
+
+@pytest.mark.parametrize("case", SIZED_CASES)
+def test_workspace_sized_by_host_lengths_is_enough(case, monkeypatch):
+    B, T, Hq, Hkv, d, lens, Lmax, tree, path = case
+    monkeypatch.setenv("HTA_FORCE_PATH", path)
+    inp = wl.random_inputs(B, T, Hq, Hkv, d, lens, seed=43, Lmax=Lmax, tree=tree)
+    t = to_device(inp, DEV)
+    mask = hta.build_mask(t["parents"])
+    ref_mask, _ = oracle.build_mask(inp.parents)
+    dims = hta.dims_of(t["q"], t["k_cache"])
+    nbytes = hta.workspace_bytes(dims, inp.cache_lens)
+    assert 0 < nbytes < hta.workspace_bytes(dims)  # the case really is below the Lmax bound
+    ws = Guarded((nbytes,), torch.uint8, fill=torch.zeros(nbytes, dtype=torch.uint8, device=DEV))
+    o = Guarded(tuple(t["q"].shape), torch.bfloat16)
+    lse = Guarded(tuple(t["q"].shape[:3]), torch.float32)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        hta.verify(t["q"], t["k_cache"], t["v_cache"], t["cache_lens"], t["k_spec"], t["v_spec"], mask,
+                   ws=ws.t, dev_err=err, out=(o.t, lse.t))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_ref, lse_ref = oracle.attention(inp.q, inp.k_cache, inp.v_cache, inp.cache_lens, inp.k_spec, inp.v_spec,
+                                      ref_mask)
+    assert_close(o.t, lse.t, o_ref, lse_ref, f"verify, sized workspace {case}")
+    assert ws.intact() and o.intact() and lse.intact()
+
+    oc = Guarded(tuple(t["q"].shape), torch.float32)
+    lc = Guarded(tuple(t["q"].shape[:3]), torch.float32)
+    hta.prefix_attn(t["q"], t["k_cache"], t["v_cache"], t["cache_lens"], ws=ws.t, dev_err=err, out=(oc.t, lc.t))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    oc_ref, lc_ref = oracle.attention(inp.q, inp.k_cache, inp.v_cache, inp.cache_lens, inp.k_spec, inp.v_spec,
+                                      np.zeros_like(ref_mask))
+    assert_close(oc.t, lc.t, oc_ref, lc_ref, f"prefix, sized workspace {case}")
+    assert ws.intact() and oc.intact() and lc.intact()
+
+
 def test_accept_commit_writes_nothing_outside_its_buffers():
     rng = np.random.default_rng(5)
     B, T, Hkv, d, Lmax = 3, 32, 2, 128, 96
