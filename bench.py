@@ -715,21 +715,22 @@ def run_drafter(args):
         workload = f"drafter cross-attention: B={B} draft query per sequence, Hq={Hq} Hkv={Hkv} d={d}, L={L}, " \
                    f"{sets} K/V sets rotated (> L2)"
     else:
-        B, T, W = 32, 1, 512
+        B, T, W, sets = 32, 1, 512, 4
         gen = torch.Generator(device=dev).manual_seed(8)
         q = torch.randn((B, T, Hq, d), device=dev, generator=gen).to(torch.bfloat16)
-        kr = torch.randn((B, Hkv, W, d), device=dev, generator=gen).to(torch.bfloat16)
-        vr = torch.randn((B, Hkv, W, d), device=dev, generator=gen).to(torch.bfloat16)
+        # one 67 MB pair of rings fits in L2: four pairs rotated, as for the cache
+        rings = [(torch.randn((B, Hkv, W, d), device=dev, generator=gen).to(torch.bfloat16),
+                  torch.randn((B, Hkv, W, d), device=dev, generator=gen).to(torch.bfloat16)) for _ in range(sets)]
         pos = torch.randint(W, 100000, (B,), dtype=torch.int32, device=dev, generator=gen)
         out = (torch.empty_like(q), torch.empty((B, T, Hq), dtype=torch.float32, device=dev))
 
         def calls():
-            for _ in range(4):
+            for kr, vr in rings:
                 hta.window_attn(q, kr, vr, pos, W, out=out)
-        per_replay = 4
+        per_replay = sets
         moved = B * W * Hkv * d * 2 * 2
         workload = f"drafter sliding-window self-attention: B={B}, T={T}, Hq={Hq} Hkv={Hkv} d={d}, " \
-                   f"window {W} over a ring of {W} slots, every window full"
+                   f"window {W} over a ring of {W} slots, every window full, {sets} ring sets rotated (> L2)"
     with torch.cuda.stream(stream):
         calls()
         stream.synchronize()

@@ -15,17 +15,22 @@
 // A draft step has few queries (often one per sequence: 4 packed rows per KV
 // head with GQA), so the CTA splits the keys, not the rows: one CTA per
 // (sequence, KV head, group of 4 packed rows). The group's visible positions
-// are walked in 64-key tiles; one thread copies each tile's K and V rows from
+// are walked in 64-key tiles; a copy warp moves each tile's K and V rows from
 // the ring into shared memory with bulk copies (two when the tile wraps past
-// the ring's end), into a ring of three stages so two tiles are in flight
-// while the current one is used. Warp w takes keys 8w .. 8w+7 of every tile: its lanes
-// split the head dimension (d/32 columns each) for the 32 (key, row) dot
-// products, and one butterfly reduce-scatter (31 shuffles) leaves lane L the
-// full score of key L / 4 and row L % 4; the softmax of a row runs over its 8
+// the ring's end), into a ring of three stages, refilling a stage as soon as
+// all eight compute warps have released it (full and empty barriers per
+// stage, no block-wide barrier per tile). Warp w takes keys 8w .. 8w+7 of
+// every tile: its lanes split the head dimension (d/32 columns each) for the
+// 32 (key, row) dot products, each lane holding pair p in slot p ^ lane, so
+// that a butterfly reduce-scatter of 31 shuffles and adds (the kept half is
+// always the low one: no selects) leaves lane L the full score of key L / 4
+// and row L % 4; the softmax of a row runs over its 8
 // lanes (one exponential per lane), and the probabilities go back to every
 // lane through shared memory for P V, accumulated on the same columns.
 // Each warp keeps an online softmax (base 2) per row; the 8 partial states
-// are merged in shared memory by the log-sum-exp rule at the end.
+// are merged in shared memory by the log-sum-exp rule at the end. The dot
+// products (two rows per instruction), the rescale and P V (two columns per
+// instruction) run on Blackwell's packed fp32 pairs.
 #include "hta_internal.cuh"
 #include "hta_launch.h"
 #include "tc_ptx.cuh"
@@ -34,25 +39,11 @@ namespace hta {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kThreads = (kWarps + 1) * 32;  // compute warps and one copy warp
 constexpr int kRows = 4;               // packed query rows per CTA
 constexpr int kTile = 64;              // keys per tile
 constexpr int kKeysPerWarp = kTile / kWarps;
 constexpr int kStages = 3;
-
-// One step of the reduce-scatter over v[0 .. 2n): the lane with bit n set
-// keeps the upper half, its partner the lower one, each adding the other's
-// copy; after the steps n = 16, 8, 4, 2, 1, v[0] of lane L is the sum over
-// all lanes of the input v[L].
-template <int n>
-__device__ __forceinline__ void scatter_step(float (&v)[32], int lane) {
-    const bool up = (lane & n) != 0;
-#pragma unroll
-    for (int q = 0; q < n; ++q) {
-        const float lo = v[q], hi = v[q + n];
-        v[q] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, n);
-    }
-}
 
 // max / sum over the 8 lanes that share lane % 4
 __device__ __forceinline__ float row_max(float v) {
@@ -64,6 +55,15 @@ __device__ __forceinline__ float row_sum(float v) {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// One step of the reduce-scatter when lane L holds pair p in slot p ^ L:
+// the pairs a lane keeps at step n are in slots [0, n), the ones it hands
+// to lane L ^ n in [n, 2n), where that lane keeps the same pairs in [0, n).
+template <int n>
+__device__ __forceinline__ void fold_step(float (&v)[32]) {
+#pragma unroll
+    for (int q = 0; q < n; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q + n], n);
 }
 
 template <int D>
@@ -83,11 +83,12 @@ struct WinSmem {
     };
     alignas(16) float prob[kWarps][32];  // a warp's probabilities of one tile, (key, row) pair L = 4 key + row
     uint64_t full[kStages];
+    uint64_t empty[kStages];  // kWarps arrivals: every compute warp is done with the stage
     int32_t status;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
     k_window_attn(const __grid_constant__ AttnParams p, const int32_t *__restrict__ pos, int32_t W, int32_t S,
                   int32_t n_rg) {
     constexpr int CPL = D / 32;  // columns per lane
@@ -129,10 +130,12 @@ __global__ void __launch_bounds__(kThreads)
         }
     };
     if (threadIdx.x == 0) {
-        for (int st = 0; st < kStages; ++st) tc::mbar_init(tc::smem_u32(&sm.full[st]), 1);
+        for (int st = 0; st < kStages; ++st) {
+            tc::mbar_init(tc::smem_u32(&sm.full[st]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.empty[st]), kWarps);
+        }
         tc::mbar_fence_init();
         sm.status = 1;
-        for (int i = 0; i < kStages - 1 && i < n_tiles; ++i) issue(i);
     }
 
     // this lane's columns of the group's queries, scaled; padding rows are zero
@@ -141,8 +144,9 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = 0; i < kRows; ++i) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) q[i][c] = 0.f;
-        if (i < nrows) {
-            const int r = r_base + i, t = r / p.G, hq = kvh * p.G + (r - t * p.G);
+        const int ir = i ^ (lane & 3);  // slot i of this lane holds row i ^ (lane % 4)
+        if (ir < nrows) {
+            const int r = r_base + ir, t = r / p.G, hq = kvh * p.G + (r - t * p.G);
             const __nv_bfloat16 *qr = p.q + (((int64_t)b * p.T + t) * p.Hq + hq) * D + lane * CPL;
 #pragma unroll
             for (int c = 0; c < CPL; c += 2) {
@@ -163,21 +167,51 @@ __global__ void __launch_bounds__(kThreads)
         for (int c = 0; c < CPL; ++c) acc[i][c] = 0.f;
     __syncthreads();  // barriers initialised
 
+    volatile int32_t *status = &sm.status;
+    if (warp == kWarps) {
+        // the copy warp: tile i goes to stage i % kStages once every compute
+        // warp has released tile i - kStages
+        if (lane == 0) {
+            for (int i = 0; i < n_tiles && *status; ++i) {
+                if (i >= kStages) {
+                    const uint64_t t0 = cycles_now();
+                    bool got = true;
+                    while (!tc::mbar_try_wait(tc::smem_u32(&sm.empty[i % kStages]), (i / kStages - 1) & 1)) {
+                        if (!*status) {
+                            got = false;
+                            break;
+                        }
+                        if (cycles_now() - t0 > kWaitLimitCycles) {
+                            flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
+                            *status = 0;
+                            got = false;
+                            break;
+                        }
+                    }
+                    if (!got) break;
+                }
+                issue(i);
+            }
+        }
+    } else {
     for (int it = 0; it < n_tiles; ++it) {
-        // tile it + 2 goes to the stage that tile it - 1 released at the end of the last iteration
-        if (threadIdx.x == 0 && it + kStages - 1 < n_tiles) issue(it + kStages - 1);
-        if (threadIdx.x == 0) {
+        bool got = true;
+        {
             const uint64_t t0 = cycles_now();
             while (!tc::mbar_try_wait(tc::smem_u32(&sm.full[it % kStages]), (it / kStages) & 1)) {
-                if (cycles_now() - t0 > kWaitLimitCycles) {
-                    flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
-                    sm.status = 0;
+                if (!*status || cycles_now() - t0 > kWaitLimitCycles) {
+                    got = false;
                     break;
                 }
             }
         }
-        __syncthreads();
-        if (!sm.status) break;
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0 && *status) {
+                flag_error(p.dev_err, HTA_DEVERR_TIMEOUT);
+                *status = 0;
+            }
+            break;
+        }
         const int64_t j0 = j_begin + (int64_t)it * kTile;
         const int n = (int)min((int64_t)kTile, j_end - j0);
         const int k_lo = warp * kKeysPerWarp, k_hi = min(n, k_lo + kKeysPerWarp);
@@ -185,7 +219,7 @@ __global__ void __launch_bounds__(kThreads)
         float v[32];
 #pragma unroll
         for (int kk = 0; kk < kKeysPerWarp; ++kk) {
-            const int key = k_lo + kk;
+            const int key = k_lo + (kk ^ (lane >> 2));  // slot kk of this lane: key kk ^ (lane / 4)
             float kf[CPL];
             if (key < k_hi) {
 #pragma unroll
@@ -199,19 +233,23 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int c = 0; c < CPL; ++c) kf[c] = 0.f;
             }
+            // rows (0, 1) and (2, 3) in pairs, columns in order
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
-            for (int i = 0; i < kRows; ++i) {
-                float d = 0.f;
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) d = fmaf(q[i][c], kf[c], d);
-                v[kk * kRows + i] = d;
+            for (int c = 0; c < CPL; ++c) {
+                tc::fma2v(d0, d1, q[0][c], q[1][c], kf[c], kf[c]);
+                tc::fma2v(d2, d3, q[2][c], q[3][c], kf[c], kf[c]);
             }
+            v[kk * kRows + 0] = d0;
+            v[kk * kRows + 1] = d1;
+            v[kk * kRows + 2] = d2;
+            v[kk * kRows + 3] = d3;
         }
-        scatter_step<16>(v, lane);
-        scatter_step<8>(v, lane);
-        scatter_step<4>(v, lane);
-        scatter_step<2>(v, lane);
-        scatter_step<1>(v, lane);
+        fold_step<16>(v);
+        fold_step<8>(v);
+        fold_step<4>(v);
+        fold_step<2>(v);
+        fold_step<1>(v);
         // lane L: key k_lo + L / 4, row L % 4; visible when P + t - W < j <= P + t
         const int64_t j = j0 + k_lo + key_l;
         const float s = (k_lo + key_l < k_hi && j <= tq_l && j > tq_l - W) ? v[0] : -INFINITY;
@@ -228,7 +266,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int i = 0; i < kRows; ++i) {
             const float a = __shfl_sync(0xffffffffu, alpha, i);  // lane i holds row i
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[i][c] *= a;
+            for (int c = 0; c < CPL; c += 2) tc::mul2s(acc[i][c], acc[i][c + 1], a);
         }
         sm.prob[warp][lane] = pr;
         __syncwarp();
@@ -247,26 +285,30 @@ __global__ void __launch_bounds__(kThreads)
                 vf[c + 1] = x.y;
             }
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                acc[0][c] = fmaf(pk.x, vf[c], acc[0][c]);
-                acc[1][c] = fmaf(pk.y, vf[c], acc[1][c]);
-                acc[2][c] = fmaf(pk.z, vf[c], acc[2][c]);
-                acc[3][c] = fmaf(pk.w, vf[c], acc[3][c]);
+            for (int c = 0; c < CPL; c += 2) {
+                tc::fma2v(acc[0][c], acc[0][c + 1], pk.x, pk.x, vf[c], vf[c + 1]);
+                tc::fma2v(acc[1][c], acc[1][c + 1], pk.y, pk.y, vf[c], vf[c + 1]);
+                tc::fma2v(acc[2][c], acc[2][c + 1], pk.z, pk.z, vf[c], vf[c + 1]);
+                tc::fma2v(acc[3][c], acc[3][c + 1], pk.w, pk.w, vf[c], vf[c + 1]);
             }
         }
         __syncwarp();  // prob is rewritten by the next tile
-        __syncthreads();  // stage it % kStages is free for tile it + kStages
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.empty[it % kStages]));  // this warp is done with the stage
     }
+    }
+    __syncthreads();  // every warp is done with the ring, which the merge reuses
 
     // merge the warps' partial softmaxes
+    if (warp < kWarps) {
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
+        for (int i = 0; i < kRows; ++i) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) sm.merge.acc[warp][i][lane * CPL + c] = acc[i][c];
-    }
-    if (lane < kRows) {  // lane i holds row i
-        sm.merge.m[warp][lane] = m_l;
-        sm.merge.l[warp][lane] = l_l;
+            for (int c = 0; c < CPL; ++c) sm.merge.acc[warp][i][lane * CPL + c] = acc[i][c];
+        }
+        if (lane < kRows) {  // lane i holds row i
+            sm.merge.m[warp][lane] = m_l;
+            sm.merge.l[warp][lane] = l_l;
+        }
     }
     __syncthreads();
     const bool ok = sm.status != 0;

@@ -450,6 +450,22 @@ __device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, f
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
+// (d0, d1) = (a0, a1) * (b0, b1) + (d0, d1), one packed instruction
+__device__ __forceinline__ void fma2v(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rd;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (d0, d1) *= (a, a)
+__device__ __forceinline__ void mul2s(float &d0, float &d1, float a) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %2};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "mul.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a));
+}
 // (s0, s1) += (a0, a1)
 __device__ __forceinline__ void add2(float &s0, float &s1, float a0, float a1) {
     asm("{\n\t.reg .b64 ra, rs;\n\t"
