@@ -819,8 +819,8 @@ def run_lspec(args):
                                f"k={k} m={m} T={T}", "real_nodes": nodes},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / peak, 5), "peak_source": peak_kind, "bytes_per_call": moved,
-                     "note": "the radix select reads the logits five times (four passes and the gather), "
-                             "from L2 after the first"},
+                     "note": "the radix select reads the logits twice (the histogram and the gather, the "
+                             "second from L2); near-equal logits too many for shared memory add passes"},
         "gpu_launches": steps * per_replay, "dtype": "int32/fp32", "data": "synthetic"}), flush=True)
 
 

@@ -21,17 +21,20 @@
 //     logits, summed by the leader over distributed shared memory), then one
 //     pass keeping the keys above the chosen digit and moving the keys at it
 //     into the leader's shared memory (four 16-byte loads in flight per
-//     thread), where three more digits
-//     resolve the threshold; the keys above it and the smallest tied ids
-//     are the k+1 survivors, ranked by a counting sort (near-equal logits
-//     too many for shared memory resolve with passes over the logits);
+//     thread). When those are few (at most kDirect: a few hundred for
+//     N(0, 1)-like logits) one counting rank over them all, key descending
+//     and id ascending, gives the k+1 survivors in order; otherwise three
+//     more digits resolve the threshold, the keys above it and the smallest
+//     tied ids are the survivors, ranked by a counting sort (near-equal
+//     logits too many for shared memory resolve with passes over the logits);
 //  2. the 1 + k queries go into a hash table in shared memory (the pages'
 //     hash-based lookup, copied to every CTA of the cluster) and every
 //     history position (a quarter per CTA) hashes its m-gram once, probes
 //     the table, confirms a hit token by token and keeps the latest start per
 //     query (atomicMax in the leader);
-//  3. branch sizes are laid out by one thread (at most 65 branches), then all
-//     threads write their nodes.
+//  3. branch r starts at min(1 + the sizes the branches before it want, T):
+//     one warp scans the (at most 65) branch sizes, then every thread writes
+//     its nodes, finding its branch by binary search.
 #include <cooperative_groups.h>
 
 #include "hta_internal.cuh"
@@ -48,6 +51,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTable = 256;  // hash slots (at least twice the queries)
 constexpr int kEqCap = 512;  // threshold ties gathered in one pass (more: the ordered scan)
 constexpr int kBuf = 1024;   // keys of the first digit held in shared memory
+constexpr int kDirect = kThreads / 2;  // candidates ranked directly (two threads per key)
 
 // order-preserving key: a larger float gives a larger key; -0 counts as +0
 // and NaN ranks below every number
@@ -238,6 +242,32 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
     }
     cl.sync();  // every candidate is in the leader
     if (rank == 0) {
+    const int32_t n_c0 = sm.n_cand, n_b0 = sm.n_buf;
+    if (in_smem && n_c0 + n_b0 <= kDirect) {
+        // every key above the first digit is a candidate and every key of the
+        // digit is in the buffer: rank them all at once, key descending and
+        // id ascending, two threads per key (each over half of the keys)
+        const int32_t n_all = n_c0 + n_b0;
+        for (int e = tid; e < n_c0; e += kThreads) {
+            sm.buf_key[n_b0 + e] = sm.cand_key[e];
+            sm.buf_id[n_b0 + e] = sm.cand_id[e];
+        }
+        __syncthreads();
+        const int e = tid >> 1, h = tid & 1;
+        int32_t pos = 0, id = 0;
+        if (e < n_all) {
+            const uint32_t ky = sm.buf_key[e];
+            id = sm.buf_id[e];
+#pragma unroll 4
+            for (int g = h; g < n_all; g += 2) {
+                const uint32_t kg = sm.buf_key[g];
+                pos += (kg > ky) || (kg == ky && sm.buf_id[g] < id);
+            }
+        }
+        pos += __shfl_xor_sync(0xffffffffu, pos, 1);
+        if (e < n_all && h == 0 && pos < K) sm.top[pos] = id;
+        __syncthreads();
+    } else {
     // the low 21 bits in three digits (8, 8, 5), over the buffer or the logits
     for (int pass = 0; pass < 3; ++pass) {
         const int shift = pass == 0 ? 13 : pass == 1 ? 5 : 0;
@@ -363,6 +393,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
         sm.top[pos] = id;
     }
     __syncthreads();
+    }
     const int32_t x1 = sm.top[0];
 
     // ---- 2. queries into the hash table (leader), one scan of the history (cluster)
@@ -430,21 +461,35 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
 
     // ---- 3. tree layout, then the nodes
     const int32_t x1 = sm.top[0];
-    if (tid == 0) {
-        int32_t used = 1;  // the root
-        for (int r = 0; r < K; ++r) {
-            int32_t len = 0;
-            if (sm.best[r] >= 0) {
-                const int64_t avail = n - ((int64_t)sm.best[r] + m);
-                len = (int32_t)min((int64_t)p.keep[r], avail);
+    if (warp == 0) {
+        // branch r starts at min(1 + the sizes wanted before it, T): a scan
+        // over the branches, 32 at a time
+        int32_t carry = 1;  // the root
+        for (int r0 = 0; r0 < K; r0 += 32) {
+            const int r = r0 + lane;
+            int32_t want = 0;
+            if (r < K) {
+                int32_t len = 0;
+                if (sm.best[r] >= 0) {
+                    const int64_t avail = n - ((int64_t)sm.best[r] + m);
+                    len = (int32_t)min((int64_t)p.keep[r], avail);
+                }
+                want = len + (r > 0 ? 1 : 0);  // a guess node heads its branch
             }
-            const int32_t want = len + (r > 0 ? 1 : 0);  // a guess node heads its branch
-            const int32_t take = min(want, p.T - used);
-            sm.br_start[r] = used;
-            sm.br_len[r] = take;
-            used += take;
+            int32_t incl = want;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += x;
+            }
+            if (r < K) {
+                const int32_t start = min(carry + incl - want, p.T), end = min(carry + incl, p.T);
+                sm.br_start[r] = start;
+                sm.br_len[r] = end - start;
+            }
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        sm.n_nodes = used;
+        if (lane == 0) sm.n_nodes = min(carry, p.T);
     }
     __syncthreads();
     const int32_t nn = sm.n_nodes;
@@ -456,8 +501,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
             pv = -1;
             tv = x1;
         } else if (v < nn) {
-            int r = 0;
-            while (r + 1 < K && sm.br_start[r + 1] <= v) ++r;  // the branch holding node v
+            int r = 0, hi = K - 1;  // the branch holding node v: the last one starting at or before v
+            while (r < hi) {
+                const int mid = (r + hi + 1) >> 1;
+                if (sm.br_start[mid] <= v) r = mid;
+                else hi = mid - 1;
+            }
             const int32_t j = v - sm.br_start[r];
             if (r > 0 && j == 0) {
                 tv = sm.top[r];  // the guess itself, a child of the root
