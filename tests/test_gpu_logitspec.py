@@ -90,6 +90,22 @@ def test_tied_logits_take_smaller_ids():
     check(logits, hist, lens, 63, 3, [3] * 64, 128)
 
 
+def test_crowded_first_digit_resolves_by_more_digits():
+    # 600 logits share the first 11-bit digit ([3, 3.5)): more than the direct
+    # rank takes, few enough for shared memory, so the threshold is resolved by
+    # three more digits; in row 1, 400 of them tie exactly at 3.25, at the threshold
+    rng = np.random.default_rng(21)
+    B, V, Lh = 2, 32000, 500
+    logits = np.clip(rng.standard_normal((B, V)), -4.0, 1.9).astype(np.float32)
+    idx = rng.choice(V, size=600, replace=False)
+    logits[0, idx] = rng.uniform(3.0, 3.5, size=600).astype(np.float32)
+    logits[1, idx[:30]] = rng.uniform(3.3, 3.5, size=30).astype(np.float32)  # 30 above the ties
+    logits[1, idx[30:200]] = rng.uniform(3.0, 3.2, size=170).astype(np.float32)
+    logits[1, idx[200:]] = 3.25  # the other 31 survivors: the smallest tied ids
+    _, hist, lens = wl.lspec_inputs(B, V, Lh, [Lh] * B, seed=13, vocab_used=40)
+    check(logits, hist, lens, 60, 3, [4] * 61, 64)
+
+
 def test_nan_logits_rank_last():
     B, V = 2, 100
     logits = np.random.default_rng(4).standard_normal((B, V)).astype(np.float32)
