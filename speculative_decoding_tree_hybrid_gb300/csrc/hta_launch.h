@@ -27,7 +27,10 @@ inline bool cooperative_requested() {
 // Launches `kern` with the n attributes in attrs[0 .. n) plus programmatic
 // stream serialization (attrs must have room for n + 1): the kernel may then
 // start while the kernel before it on the stream is still running, and waits
-// for it (griddep_wait) before reading any input. If the runtime rejects that
+// for it (griddep_wait) before reading what that kernel writes. The mask
+// build is the only kernel here that lets its dependent start early, and only
+// once every kernel before it has finished, so the attention kernels wait
+// only before reading the mask. If the runtime rejects that
 // attribute with the others, the launch is repeated without it, and so are
 // all later launches of the process.
 template <typename... KArgs, typename... Args>

@@ -27,11 +27,13 @@ __global__ void __launch_bounds__(HTA_TMAX) k_build_mask(const int32_t *__restri
     __shared__ int bad_s;
     const int b = blockIdx.x, i = threadIdx.x;
     const int32_t *par = parents + (int64_t)b * T;
-    tc::griddep_launch_dependents();  // the attention launch may set up meanwhile
     // launched as a programmatic dependent: the kernel before it (often the
     // attention of the previous step, which reads the mask) has finished and
     // its memory is visible from here on
     tc::griddep_wait();
+    // only now may the attention launch start: every kernel before this one
+    // has finished, so the attention waits for nothing but this mask
+    tc::griddep_launch_dependents();
     if (i == 0) bad_s = 0;
     __syncthreads();
     int32_t pi = -1;

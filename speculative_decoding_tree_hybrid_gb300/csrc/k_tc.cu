@@ -238,6 +238,7 @@ __device__ void mma_issuer(const AttnParams &p, TcShared &sh, uint32_t sQ, uint3
 template <int kStages>
 __device__ void softmax_wg(const AttnParams &p, TcShared &sh, uint32_t ring, uint32_t tmem,
                            int h, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+    griddep_wait();  // the mask build before this launch has finished
     volatile int32_t *abort = &sh.abort;
     const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;  // row of this half == TMEM lane
@@ -453,9 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
         tc_fence_before();
     }
-    // everything above reads no input: with a programmatic dependent launch
-    // it overlaps the kernel before this one on the stream
-    griddep_wait();
+    // The only kernel that lets this one start before it has finished is the
+    // mask build, which writes the tree mask alone and lets it start only
+    // once every kernel before the mask build has finished: the softmax warps,
+    // which read the mask, wait for it; everything else starts at once
     build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;

@@ -275,6 +275,7 @@ __device__ void mma_issuer(const AttnParams &p, Tc2Shared &sh, uint32_t sQ, uint
 template <int kStages>
 __device__ void softmax_wg(const AttnParams &p, Tc2Shared &sh, uint32_t ring, uint32_t tmem, uint32_t rank,
                            uint32_t worker, const int32_t *lens_s, const int64_t *pre_s, int64_t u0, int64_t u1) {
+    griddep_wait();  // the mask build before this launch has finished
     volatile int32_t *abort = &sh.abort;
     const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
     const int row = wq * 32 + lane;  // row of this sub-group == TMEM lane
@@ -588,9 +589,10 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
     // every CTA's barriers exist before any multicasts into another: the
     // cluster barrier's round trip overlaps the schedule below
     cluster_arrive();
-    // everything above reads no input: with a programmatic dependent launch
-    // it overlaps the kernel before this one on the stream
-    griddep_wait();
+    // The only kernel that lets this one start before it has finished is the
+    // mask build, which writes the tree mask alone and lets it start only
+    // once every kernel before the mask build has finished: the softmax warps,
+    // which read the mask, wait for it; everything else starts at once
     build_schedule(p, lens_s, pre_s, lo_s);  // ends with __syncthreads
     cluster_wait();
     tc_fence_after();
