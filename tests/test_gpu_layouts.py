@@ -93,6 +93,27 @@ def test_verify_layout_bit_identical(contiguous, case, order, P):
     assert_close(o, lse, *ref, f"{case} {order} P={P}")
 
 
+@pytest.mark.parametrize("order,P", [("hnd", 16), ("nhd", 64), ("nhd", 0)])
+@pytest.mark.parametrize("case", list(CASES))
+def test_verify_layout_in_workspace_sized_by_host_lengths(contiguous, case, order, P):
+    # a workspace of exactly hta_verify_workspace_bytes(dims, lens): the call
+    # runs with the split-KV workers it holds, within the oracle's tolerance
+    inp, t, mask, o0, lse0, ref, path = contiguous[case]
+    s = stored(inp, order, P)
+    dims, _, _ = hta._kv_layout(t["q"], s["k_cache"], s["v_cache"], t["cache_lens"], order, s["block_table"])
+    nbytes = hta.workspace_bytes(dims, inp.cache_lens)
+    assert 0 < nbytes <= hta.workspace_bytes(dims)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        o, lse = hta.verify_kv(t["q"], s["k_cache"], s["v_cache"], t["cache_lens"], s["k_spec"], s["v_spec"],
+                               mask, order=order, block_table=s["block_table"], ws=ws, dev_err=err)
+    torch.cuda.synchronize()
+    assert hta.last_path() == path
+    assert int(err.item()) == 0
+    assert_close(o, lse, *ref, f"{case} {order} P={P}, sized workspace")
+
+
 @pytest.mark.parametrize("order,P", [("hnd", 16), ("nhd", 128), ("nhd", 0)])
 def test_prefix_attn_layout_cross_attention(oracle_mod, order, P):
     """The draft model's cross-attention (a few queries over the target's
