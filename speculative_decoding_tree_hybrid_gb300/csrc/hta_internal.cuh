@@ -340,6 +340,92 @@ __device__ __forceinline__ SegPieces seg_pieces(const AttnParams &p, uint32_t se
     return r;
 }
 
+// Folds records first, first + step, ... of one row (batches of KB, every
+// load of a batch issued before any arithmetic: one round trip per batch; KB
+// is set by the kernel's register budget) into the running (M, den, acc) of
+// this thread's columns col0 + 64 h + e.
+template <int D, int KB>
+__device__ __forceinline__ void fold_records(const float *row, size_t rec_stride, int32_t nrec, bool dense,
+                                             const int64_t *lo_s, int32_t cf, int32_t subs, int col0,
+                                             int32_t first, int32_t step, float &M, float &den,
+                                             float (&acc)[D / 16]) {
+    constexpr int HPL = D / 16;
+    for (int32_t k0 = first; k0 < nrec; k0 += step) {
+        float2 ml[KB];
+        float4 v[KB][HPL / 4];
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            const int32_t k = k0 + j;
+            const bool has = k < nrec && (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1]);
+            const float *rec = row + (size_t)k * rec_stride;
+            ml[j] = has ? __ldcg(reinterpret_cast<const float2 *>(rec + D)) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int c = 0; c < HPL / 4; ++c)
+                v[j][c] = has ? __ldcg(reinterpret_cast<const float4 *>(rec + col0 + c * 64))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            if (ml[j].x > M) {  // a larger running max: scale what has been summed so far
+                const float s = M == -INFINITY ? 0.f : tc::ex2(M - ml[j].x);
+                den *= s;
+#pragma unroll
+                for (int c = 0; c < HPL; ++c) acc[c] *= s;
+                M = ml[j].x;
+            }
+            const float w = ml[j].x == -INFINITY ? 0.f : tc::ex2(ml[j].x - M);  // no record: no weight
+            den = fmaf(w, ml[j].y, den);
+#pragma unroll
+            for (int c = 0; c < HPL / 4; ++c) {
+                acc[4 * c] = fmaf(w, v[j][c].x, acc[4 * c]);
+                acc[4 * c + 1] = fmaf(w, v[j][c].y, acc[4 * c + 1]);
+                acc[4 * c + 2] = fmaf(w, v[j][c].z, acc[4 * c + 2]);
+                acc[4 * c + 3] = fmaf(w, v[j][c].w, acc[4 * c + 3]);
+            }
+        }
+    }
+}
+
+// Normalises this thread's columns of one output row and writes them (and, in
+// column chunk 0, the row's LSE); ok = false writes NaN.
+template <int D>
+__device__ __forceinline__ void write_item(const AttnParams &p, bool ok, float M, float den, float (&acc)[D / 16],
+                                           int64_t out_row, int col0, int ch) {
+    constexpr int HPL = D / 16;
+    float lse, inv;
+    if (!ok) {
+        lse = __int_as_float(0x7fc00000);
+        inv = __int_as_float(0x7fc00000);
+    } else if (den > 0.f) {
+        float l2;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(den));
+        lse = (M + l2) * kLn2;
+        inv = __frcp_rn(den);
+    } else {
+        lse = -INFINITY;  // no visible key: empty softmax
+        inv = 0.f;
+    }
+    if (p.out_fp32) {
+        float *op = (float *)p.out_o + out_row * D + col0;
+#pragma unroll
+        for (int c = 0; c < HPL; c += 4)
+            *reinterpret_cast<float4 *>(op + c * 16) =
+                make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
+    } else {
+        __nv_bfloat16 *op = (__nv_bfloat16 *)p.out_o + out_row * D + col0;
+#pragma unroll
+        for (int c = 0; c < HPL; c += 4) {
+            const __nv_bfloat162 x = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
+            const __nv_bfloat162 y = __floats2bfloat162_rn(acc[c + 2] * inv, acc[c + 3] * inv);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t *>(&x);
+            u.y = *reinterpret_cast<const uint32_t *>(&y);
+            *reinterpret_cast<uint2 *>(op + c * 16) = u;
+        }
+    }
+    if (ch == 0) p.out_lse[out_row] = lse;
+}
+
 // Merges rows [lo, lo + nrows) of segment seg over its pieces and writes O
 // and LSE: one thread per (row, column chunk) reads the records of every
 // piece straight from global memory (one round trip of independent loads;
@@ -351,7 +437,9 @@ __device__ __forceinline__ SegPieces seg_pieces(const AttnParams &p, uint32_t se
 //   2^(M_old - M_new); w_k = 2^(m_k - M), den += w_k l_k, acc += w_k O_k;
 //   O = acc / den, LSE = (M + log2 den) ln 2.
 // The result depends on the piece order only, not on which CTA merges.
-// ok = false writes NaN (a piece is missing).
+// ok = false writes NaN (a piece is missing). In kernels whose batches are
+// small (KB < 8), rows split over many workers are merged by up to 16
+// threads per (row, column chunk), each over every S-th batch.
 template <int D, int KB>
 __device__ inline void merge_rows(const AttnParams &p, const int64_t *lo_s, uint32_t seg, const SegPieces &pc,
                                   uint32_t lo, uint32_t nrows_run, bool ok) {
@@ -368,88 +456,62 @@ __device__ inline void merge_rows(const AttnParams &p, const int64_t *lo_s, uint
     // record x of piece k, row lr: ws_rec + ((seg + cf + k) * subs + x) * rows_pg + lr) * REC
     const float *const rec0 = p.ws_rec + ((size_t)(seg + cf) * subs * rows_pg) * REC;
     const size_t rec_stride = (size_t)rows_pg * REC;  // floats between consecutive records
-    for (int32_t item = threadIdx.x; item < (int32_t)nrows_run * NCH; item += blockDim.x) {
-        const int32_t i = item / NCH, ch = item - i * NCH;
-        const uint32_t lr = lo + (uint32_t)i;
-        const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
-        const uint32_t t = r / G, hq = kvh * G + (r - t * G);
-        const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
-        const int col0 = ch * 4;  // this thread's columns: col0 + 64 h + e, h < HPL / 4, e < 4
-        float M = -INFINITY, den = 0.f, acc[HPL];
+    const int32_t items = (int32_t)nrows_run * NCH;
+    if constexpr (KB >= 8) {
+        // one thread per item: a batch holds every piece of the shapes these kernels take
+        for (int32_t item = threadIdx.x; item < items; item += blockDim.x) {
+            const int32_t i = item / NCH, ch = item - i * NCH;
+            const uint32_t lr = lo + (uint32_t)i;
+            const uint32_t r = rg * rows_pg + lr;  // packed row within the KV head
+            const uint32_t t = r / G, hq = kvh * G + (r - t * G);
+            const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
+            const int col0 = ch * 4;  // this thread's columns: col0 + 64 h + e, h < HPL / 4, e < 4
+            float M = -INFINITY, den = 0.f, acc[HPL];
 #pragma unroll
-        for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
-        if (ok) {
-            const float *row = rec0 + (size_t)lr * REC;
-            // records in batches of KB, every load of a batch issued before any
-            // arithmetic: one round trip per batch (KB is set by the kernel's
-            // register budget)
-            for (int32_t k0 = 0; k0 < nrec; k0 += KB) {
-                float2 ml[KB];
-                float4 v[KB][HPL / 4];
+            for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
+            if (ok) fold_records<D, KB>(rec0 + (size_t)lr * REC, rec_stride, nrec, dense, lo_s, cf, subs, col0, 0, KB, M,
+                                        den, acc);
+            write_item<D>(p, ok, M, den, acc, out_row, col0, ch);
+        }
+    } else {
+        // Few items and many records (rows split over many workers): S threads
+        // per item, neighbouring lanes, each folding every S-th batch of
+        // records; their partial states are combined by shuffles in a fixed
+        // order, so the result is still deterministic.
+        int32_t S = 1;
+        while (S < 16 && items * S * 2 <= (int32_t)blockDim.x && S * KB < nrec) S *= 2;
+        const int32_t span = (items * S + 31) & ~31;  // whole warps: every lane takes part in the shuffles
+        for (int32_t slot = threadIdx.x; slot < span; slot += blockDim.x) {
+            const int32_t item = slot / S, sub = slot - item * S;
+            const bool live = item < items;
+            const int32_t i = live ? item / NCH : 0, ch = live ? item - i * NCH : 0;
+            const uint32_t lr = lo + (uint32_t)i;
+            const uint32_t r = rg * rows_pg + lr;
+            const uint32_t t = r / G, hq = kvh * G + (r - t * G);
+            const int64_t out_row = ((int64_t)b * T + t) * Hq + hq;
+            const int col0 = ch * 4;
+            float M = -INFINITY, den = 0.f, acc[HPL];
 #pragma unroll
-                for (int j = 0; j < KB; ++j) {
-                    const int32_t k = k0 + j;
-                    const bool has = k < nrec && (dense || lo_s[cf + k / subs] != lo_s[cf + k / subs + 1]);
-                    const float *rec = row + (size_t)k * rec_stride;
-                    ml[j] = has ? __ldcg(reinterpret_cast<const float2 *>(rec + D)) : make_float2(-INFINITY, 0.f);
+            for (int c = 0; c < HPL; ++c) acc[c] = 0.f;
+            if (ok && live)
+                fold_records<D, KB>(rec0 + (size_t)lr * REC, rec_stride, nrec, dense, lo_s, cf, subs, col0, sub * KB,
+                                    S * KB, M, den, acc);
+            for (int o = S >> 1; o > 0; o >>= 1) {  // S is the same in every thread
+                const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+                const float d2 = __shfl_xor_sync(0xffffffffu, den, o);
+                const float Mn = fmaxf(M, M2);
+                const float s1 = M == -INFINITY ? 0.f : tc::ex2(M - Mn);
+                const float s2 = M2 == -INFINITY ? 0.f : tc::ex2(M2 - Mn);
+                den = fmaf(den, s1, d2 * s2);
 #pragma unroll
-                    for (int c = 0; c < HPL / 4; ++c)
-                        v[j][c] = has ? __ldcg(reinterpret_cast<const float4 *>(rec + col0 + c * 64))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = 0; c < HPL; ++c) {
+                    const float a2 = __shfl_xor_sync(0xffffffffu, acc[c], o);
+                    acc[c] = fmaf(acc[c], s1, a2 * s2);
                 }
-#pragma unroll
-                for (int j = 0; j < KB; ++j) {
-                    if (ml[j].x > M) {  // a larger running max: scale what has been summed so far
-                        const float s = M == -INFINITY ? 0.f : tc::ex2(M - ml[j].x);
-                        den *= s;
-#pragma unroll
-                        for (int c = 0; c < HPL; ++c) acc[c] *= s;
-                        M = ml[j].x;
-                    }
-                    const float w = ml[j].x == -INFINITY ? 0.f : tc::ex2(ml[j].x - M);  // no record: no weight
-                    den = fmaf(w, ml[j].y, den);
-#pragma unroll
-                    for (int c = 0; c < HPL / 4; ++c) {
-                        acc[4 * c] = fmaf(w, v[j][c].x, acc[4 * c]);
-                        acc[4 * c + 1] = fmaf(w, v[j][c].y, acc[4 * c + 1]);
-                        acc[4 * c + 2] = fmaf(w, v[j][c].z, acc[4 * c + 2]);
-                        acc[4 * c + 3] = fmaf(w, v[j][c].w, acc[4 * c + 3]);
-                    }
-                }
+                M = Mn;
             }
+            if (live && sub == 0) write_item<D>(p, ok, M, den, acc, out_row, col0, ch);
         }
-        float lse, inv;
-        if (!ok) {
-            lse = __int_as_float(0x7fc00000);
-            inv = __int_as_float(0x7fc00000);
-        } else if (den > 0.f) {
-            float l2;
-            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(den));
-            lse = (M + l2) * kLn2;
-            inv = __frcp_rn(den);
-        } else {
-            lse = -INFINITY;  // no visible key: empty softmax
-            inv = 0.f;
-        }
-        if (p.out_fp32) {
-            float *op = (float *)p.out_o + out_row * D + col0;
-#pragma unroll
-            for (int c = 0; c < HPL; c += 4)
-                *reinterpret_cast<float4 *>(op + c * 16) =
-                    make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
-        } else {
-            __nv_bfloat16 *op = (__nv_bfloat16 *)p.out_o + out_row * D + col0;
-#pragma unroll
-            for (int c = 0; c < HPL; c += 4) {
-                const __nv_bfloat162 x = __floats2bfloat162_rn(acc[c] * inv, acc[c + 1] * inv);
-                const __nv_bfloat162 y = __floats2bfloat162_rn(acc[c + 2] * inv, acc[c + 3] * inv);
-                uint2 u;
-                u.x = *reinterpret_cast<const uint32_t *>(&x);
-                u.y = *reinterpret_cast<const uint32_t *>(&y);
-                *reinterpret_cast<uint2 *>(op + c * 16) = u;
-            }
-        }
-        if (ch == 0) p.out_lse[out_row] = lse;
     }
 }
 
