@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();  // barriers initialised
 
     volatile int32_t *status = &sm.status;
+    int n_issued = 0;  // copy warp, lane 0: tiles whose copies were issued
     if (warp == kWarps) {
         // the copy warp: tile i goes to stage i % kStages once every compute
         // warp has released tile i - kStages
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (!got) break;
                 }
                 issue(i);
+                n_issued = i + 1;
             }
         }
     } else {
@@ -297,6 +299,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     }
     __syncthreads();  // every warp is done with the ring, which the merge reuses
+    if (!*status) {  // the same in every thread from here on
+        // a wait gave up: copies may still be landing in the ring. Wait
+        // (bounded) for the latest tile of each stage, whose phase is the only
+        // one that can still be open.
+        if (warp == kWarps && lane == 0) {
+            for (int i = max(0, n_issued - kStages); i < n_issued; ++i) {
+                const uint64_t t0 = cycles_now();
+                while (!tc::mbar_try_wait(tc::smem_u32(&sm.full[i % kStages]), (i / kStages) & 1))
+                    if (cycles_now() - t0 > kWaitLimitCycles) break;
+            }
+        }
+        __syncthreads();
+    }
 
     // merge the warps' partial softmaxes
     if (warp < kWarps) {
