@@ -28,10 +28,18 @@ oracle.build()
 DEV = torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("path", ["tc2", "tc", "cc"])
-def test_barrier_timeout_flags_nan_and_recovers(path, monkeypatch):
+# (B, T, lens): 256 packed rows per KV head; and one query per sequence (4
+# rows per KV head, each split over many workers: several threads merge a row)
+SHAPES = {"tree64": (2, 64, [6000, 2500]), "one_query": (1, 1, [9000])}
+
+
+@pytest.mark.parametrize("path,shape", [("tc2", "tree64"), ("tc", "tree64"), ("cc", "tree64"),
+                                        ("tc", "one_query"), ("cc", "one_query")])
+def test_barrier_timeout_flags_nan_and_recovers(path, shape, monkeypatch):
     monkeypatch.setenv("HTA_FORCE_PATH", path)
-    inp = wl.random_inputs(2, 64, 32, 8, 128, [6000, 2500], seed=31, tree="window8_depth8")
+    B, T, lens = SHAPES[shape]
+    tree = "window8_depth8" if T > 1 else "uniform"
+    inp = wl.random_inputs(B, T, 32, 8, 128, lens, seed=31, tree=tree)
     t = to_device(inp, DEV)
     mask = hta.build_mask(t["parents"])
     ref_mask, _ = oracle.build_mask(inp.parents)
