@@ -268,131 +268,131 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
         if (e < n_all && h == 0 && pos < K) sm.top[pos] = id;
         __syncthreads();
     } else {
-    // the low 21 bits in three digits (8, 8, 5), over the buffer or the logits
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 13 : pass == 1 ? 5 : 0;
-        const uint32_t dmask = pass == 2 ? 31u : 255u;
-        for (int i = tid; i < kWarps * 256; i += kThreads) (&sm.hist[0][0])[i] = 0u;
-        __syncthreads();
-        const uint32_t prefix = sm.prefix, mask = sm.mask;
-        auto count = [&](int, uint32_t key) {
-            if ((key & mask) == prefix) atomicAdd(&sm.hist[warp][(key >> shift) & dmask], 1u);
-        };
+        // the low 21 bits in three digits (8, 8, 5), over the buffer or the logits
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = pass == 0 ? 13 : pass == 1 ? 5 : 0;
+            const uint32_t dmask = pass == 2 ? 31u : 255u;
+            for (int i = tid; i < kWarps * 256; i += kThreads) (&sm.hist[0][0])[i] = 0u;
+            __syncthreads();
+            const uint32_t prefix = sm.prefix, mask = sm.mask;
+            auto count = [&](int, uint32_t key) {
+                if ((key & mask) == prefix) atomicAdd(&sm.hist[warp][(key >> shift) & dmask], 1u);
+            };
+            if (in_smem) {
+                for (int e = tid; e < sm.n_buf; e += kThreads) count(0, sm.buf_key[e]);
+            } else {
+                for_each_key(lg, p.V, count);
+            }
+            __syncthreads();
+            if (tid < 256) {  // fold the warps' histograms into row 0
+                uint32_t c = 0;
+                for (int w = 0; w < kWarps; ++w) c += sm.hist[w][tid];
+                sm.hist[0][tid] = c;
+            }
+            __syncthreads();
+            // the digit holding the remaining-th largest key, from the top
+            const int32_t need_in = sm.remaining;
+            __syncthreads();
+            select_digit(&sm.hist[0][0], (int)dmask + 1, need_in, sm.wcount, &sm.sel_d, &sm.remaining);
+            if (tid == 0) {
+                const int32_t d = sm.sel_d;
+                if (pass == 2) sm.eq_total = (int32_t)sm.hist[0][d];  // every key equal to the threshold
+                sm.prefix |= (uint32_t)d << shift;
+                sm.mask |= dmask << shift;
+            }
+            __syncthreads();
+        }
+        const uint32_t thr = sm.prefix;
+        const int32_t need_eq = sm.remaining;
         if (in_smem) {
-            for (int e = tid; e < sm.n_buf; e += kThreads) count(0, sm.buf_key[e]);
+            // the buffer's keys above the threshold, then the need_eq smallest tied ids
+            for (int e = tid; e < sm.n_buf; e += kThreads) {
+                const uint32_t key = sm.buf_key[e];
+                if (key > thr) {
+                    const int slot = atomicAdd(&sm.n_cand, 1);
+                    sm.cand_key[slot] = key;
+                    sm.cand_id[slot] = sm.buf_id[e];
+                } else if (key == thr) {
+                    sm.eq_id[atomicAdd(&sm.n_eq, 1)] = sm.buf_id[e];
+                }
+            }
+            __syncthreads();
+        } else if (sm.eq_total <= kEqCap) {
+            // one more global pass: the keys above the threshold below the first
+            // digit were not kept yet, and every tie at it
+            const uint32_t d1 = thr >> 21;
+            for_each_key(lg, p.V, [&](int i, uint32_t key) {
+                if (key > thr && (key >> 21) == d1) {
+                    const int slot = atomicAdd(&sm.n_cand, 1);
+                    sm.cand_key[slot] = key;
+                    sm.cand_id[slot] = i;
+                } else if (key == thr) {
+                    sm.eq_id[atomicAdd(&sm.n_eq, 1)] = i;
+                }
+            });
+            __syncthreads();
+        }
+        if (in_smem || sm.eq_total <= kEqCap) {
+            const int n_eq = sm.n_eq, base = sm.n_cand;
+            for (int e = tid; e < n_eq; e += kThreads) {
+                const int32_t id = sm.eq_id[e];
+                int32_t rank = 0;
+                for (int f = 0; f < n_eq; ++f) rank += sm.eq_id[f] < id;
+                if (rank < need_eq) {
+                    sm.cand_key[base + rank] = thr;
+                    sm.cand_id[base + rank] = id;
+                }
+            }
+            __syncthreads();
         } else {
-            for_each_key(lg, p.V, count);
-        }
-        __syncthreads();
-        if (tid < 256) {  // fold the warps' histograms into row 0
-            uint32_t c = 0;
-            for (int w = 0; w < kWarps; ++w) c += sm.hist[w][tid];
-            sm.hist[0][tid] = c;
-        }
-        __syncthreads();
-        // the digit holding the remaining-th largest key, from the top
-        const int32_t need_in = sm.remaining;
-        __syncthreads();
-        select_digit(&sm.hist[0][0], (int)dmask + 1, need_in, sm.wcount, &sm.sel_d, &sm.remaining);
-        if (tid == 0) {
-            const int32_t d = sm.sel_d;
-            if (pass == 2) sm.eq_total = (int32_t)sm.hist[0][d];  // every key equal to the threshold
-            sm.prefix |= (uint32_t)d << shift;
-            sm.mask |= dmask << shift;
-        }
-        __syncthreads();
-    }
-    const uint32_t thr = sm.prefix;
-    const int32_t need_eq = sm.remaining;
-    if (in_smem) {
-        // the buffer's keys above the threshold, then the need_eq smallest tied ids
-        for (int e = tid; e < sm.n_buf; e += kThreads) {
-            const uint32_t key = sm.buf_key[e];
-            if (key > thr) {
-                const int slot = atomicAdd(&sm.n_cand, 1);
-                sm.cand_key[slot] = key;
-                sm.cand_id[slot] = sm.buf_id[e];
-            } else if (key == thr) {
-                sm.eq_id[atomicAdd(&sm.n_eq, 1)] = sm.buf_id[e];
-            }
-        }
-        __syncthreads();
-    } else if (sm.eq_total <= kEqCap) {
-        // one more global pass: the keys above the threshold below the first
-        // digit were not kept yet, and every tie at it
-        const uint32_t d1 = thr >> 21;
-        for_each_key(lg, p.V, [&](int i, uint32_t key) {
-            if (key > thr && (key >> 21) == d1) {
-                const int slot = atomicAdd(&sm.n_cand, 1);
-                sm.cand_key[slot] = key;
-                sm.cand_id[slot] = i;
-            } else if (key == thr) {
-                sm.eq_id[atomicAdd(&sm.n_eq, 1)] = i;
-            }
-        });
-        __syncthreads();
-    }
-    if (in_smem || sm.eq_total <= kEqCap) {
-        const int n_eq = sm.n_eq, base = sm.n_cand;
-        for (int e = tid; e < n_eq; e += kThreads) {
-            const int32_t id = sm.eq_id[e];
-            int32_t rank = 0;
-            for (int f = 0; f < n_eq; ++f) rank += sm.eq_id[f] < id;
-            if (rank < need_eq) {
-                sm.cand_key[base + rank] = thr;
-                sm.cand_id[base + rank] = id;
-            }
-        }
-        __syncthreads();
-    } else {
-        for (int i0 = 0; i0 < p.V; i0 += kThreads) {
-            // many ties: the ordered scan takes the need_eq smallest tied ids,
-            // counting ties chunk by chunk in id order (keys above the
-            // threshold inside the first digit join on the way)
-            const int i = i0 + tid;
-            const uint32_t key = i < p.V ? fkey(lg[i]) : 0u;
-            if (i < p.V && key > thr && (key >> 21) == (thr >> 21)) {
-                const int slot = atomicAdd(&sm.n_cand, 1);
-                sm.cand_key[slot] = key;
-                sm.cand_id[slot] = i;
-            }
-            const int32_t eq_base = sm.eq_base;  // uniform: written only between the barriers below
-            if (eq_base < need_eq) {
-                const bool eq = i < p.V && key == thr;
-                const unsigned bal = __ballot_sync(0xffffffffu, eq);
-                if (lane == 0) sm.wcount[warp] = __popc(bal);
-                __syncthreads();
-                int32_t before = eq_base;
-                for (int w = 0; w < warp; ++w) before += sm.wcount[w];
-                const int32_t rank = before + __popc(bal & ((1u << lane) - 1u));
-                if (eq && rank < need_eq) {
+            for (int i0 = 0; i0 < p.V; i0 += kThreads) {
+                // many ties: the ordered scan takes the need_eq smallest tied ids,
+                // counting ties chunk by chunk in id order (keys above the
+                // threshold inside the first digit join on the way)
+                const int i = i0 + tid;
+                const uint32_t key = i < p.V ? fkey(lg[i]) : 0u;
+                if (i < p.V && key > thr && (key >> 21) == (thr >> 21)) {
                     const int slot = atomicAdd(&sm.n_cand, 1);
                     sm.cand_key[slot] = key;
                     sm.cand_id[slot] = i;
                 }
-                __syncthreads();
-                if (tid == 0) {
-                    int32_t tot = 0;
-                    for (int w = 0; w < kWarps; ++w) tot += sm.wcount[w];
-                    sm.eq_base = eq_base + tot;
+                const int32_t eq_base = sm.eq_base;  // uniform: written only between the barriers below
+                if (eq_base < need_eq) {
+                    const bool eq = i < p.V && key == thr;
+                    const unsigned bal = __ballot_sync(0xffffffffu, eq);
+                    if (lane == 0) sm.wcount[warp] = __popc(bal);
+                    __syncthreads();
+                    int32_t before = eq_base;
+                    for (int w = 0; w < warp; ++w) before += sm.wcount[w];
+                    const int32_t rank = before + __popc(bal & ((1u << lane) - 1u));
+                    if (eq && rank < need_eq) {
+                        const int slot = atomicAdd(&sm.n_cand, 1);
+                        sm.cand_key[slot] = key;
+                        sm.cand_id[slot] = i;
+                    }
+                    __syncthreads();
+                    if (tid == 0) {
+                        int32_t tot = 0;
+                        for (int w = 0; w < kWarps; ++w) tot += sm.wcount[w];
+                        sm.eq_base = eq_base + tot;
+                    }
+                    __syncthreads();
                 }
-                __syncthreads();
             }
+            __syncthreads();
+        }
+        // rank sort: key descending, id ascending
+        if (tid < K) {
+            const uint32_t ky = sm.cand_key[tid];
+            const int32_t id = sm.cand_id[tid];
+            int32_t pos = 0;
+            for (int j = 0; j < K; ++j) {
+                const uint32_t kj = sm.cand_key[j];
+                pos += (kj > ky) || (kj == ky && sm.cand_id[j] < id);
+            }
+            sm.top[pos] = id;
         }
         __syncthreads();
-    }
-    // rank sort: key descending, id ascending
-    if (tid < K) {
-        const uint32_t ky = sm.cand_key[tid];
-        const int32_t id = sm.cand_id[tid];
-        int32_t pos = 0;
-        for (int j = 0; j < K; ++j) {
-            const uint32_t kj = sm.cand_key[j];
-            pos += (kj > ky) || (kj == ky && sm.cand_id[j] < id);
-        }
-        sm.top[pos] = id;
-    }
-    __syncthreads();
     }
     const int32_t x1 = sm.top[0];
 
