@@ -29,8 +29,9 @@
 //     logits too many for shared memory resolve with passes over the logits);
 //  2. the 1 + k queries go into a hash table in shared memory (the pages'
 //     hash-based lookup, copied to every CTA of the cluster) and every
-//     history position (a quarter per CTA) hashes its m-gram once, probes
-//     the table, confirms a hit token by token and keeps the latest start per
+//     history position (a quarter per CTA) hashes its m-gram once, tests a
+//     bitmap of the query hashes (most positions stop there), probes the
+//     table, confirms a hit token by token and keeps the latest start per
 //     query (atomicMax in the leader);
 //  3. branch r starts at min(1 + the sizes the branches before it want, T):
 //     one warp scans the (at most 65) branch sizes, then every thread writes
@@ -49,6 +50,7 @@ constexpr int kThreads = 512;
 constexpr int kCtas = 4;  // CTAs per sequence: a thread-block cluster
 constexpr int kWarps = kThreads / 32;
 constexpr int kTable = 256;  // hash slots (at least twice the queries)
+constexpr int kBloom = 4096; // bits of the query-hash bitmap that screens history positions
 constexpr int kEqCap = 512;  // threshold ties gathered in one pass (more: the ordered scan)
 constexpr int kBuf = 1024;   // keys of the first digit held in shared memory
 constexpr int kDirect = kThreads / 2;  // candidates ranked directly (two threads per key)
@@ -162,6 +164,7 @@ struct LspecSmem {
     int32_t q_ok[HTA_LSPEC_KMAX + 1];
     int32_t best[HTA_LSPEC_KMAX + 1];
     uint32_t slot_hash[kTable];
+    uint32_t bloom[kBloom / 32];  // bit h % kBloom set for every query hash h
     int32_t slot_q[kTable];
     int32_t br_start[HTA_LSPEC_KMAX + 1], br_len[HTA_LSPEC_KMAX + 1];
     int32_t wcount[kWarps];
@@ -398,6 +401,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
 
     // ---- 2. queries into the hash table (leader), one scan of the history (cluster)
     for (int i = tid; i < kTable; i += kThreads) sm.slot_q[i] = -1;
+    for (int i = tid; i < kBloom / 32; i += kThreads) sm.bloom[i] = 0u;
     if (tid < K) {
         // query 0: the last m-1 history tokens and x1; query r: the last m-2, x1, guess r
         const int r = tid, hist_part = r == 0 ? m - 1 : m - 2;
@@ -416,6 +420,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
         uint32_t s = h & (kTable - 1);
         while (atomicCAS(&sm.slot_q[s], -1, tid) != -1) s = (s + 1) & (kTable - 1);
         sm.slot_hash[s] = h;
+        atomicOr(&sm.bloom[(h >> 5) & (kBloom / 32 - 1)], 1u << (h & 31));
     }
     }  // leader
     cl.sync();  // the queries and their table are in the leader
@@ -424,6 +429,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
             sm.slot_q[i] = lead.slot_q[i];
             sm.slot_hash[i] = lead.slot_hash[i];
         }
+        for (int i = tid; i < kBloom / 32; i += kThreads) sm.bloom[i] = lead.bloom[i];
         for (int i = tid; i < K * HTA_LSPEC_MMAX; i += kThreads) (&sm.q[0][0])[i] = (&lead.q[0][0])[i];
     }
     __syncthreads();
@@ -446,6 +452,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
             const int64_t s = s0 + (int64_t)u * kThreads;
             if (s >= s_hi) continue;
             const uint32_t h = gram_hash(g[u], m);
+            // most positions match no query's hash: one bitmap test, no probe
+            if (!((sm.bloom[(h >> 5) & (kBloom / 32 - 1)] >> (h & 31)) & 1u)) continue;
             for (uint32_t t = h & (kTable - 1); sm.slot_q[t] >= 0; t = (t + 1) & (kTable - 1)) {
                 if (sm.slot_hash[t] != h) continue;
                 const int r = sm.slot_q[t];
